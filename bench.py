@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""KDA hot-path benchmark: chunk-32 prefill + T=1 decode on GB300, one JSON line.
+
+One step = one kda_prefill call over the prefill workload followed by one kda_decode
+call over the decode workload (both rows of the hot path), inputs resident in HBM.
+Default workload: prefill 1 x 8192 tokens, H = 8, lower bound -5, FP32 initial state
+N(0, 0.02); decode H = 8, 4096 rows against a 16384-slot FP32 pool, scattered
+unique slots. L2 is flushed (a 512 MiB write) between steps, outside the timed kernel
+segments. ``value`` is prefill tokens*heads/s over the prefill kernel time; decode
+rows*heads/s is reported beside it; ``roofline`` is the kernel with the larger time
+share (the other kernel's roofline sits in its own object).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--prefill prefill_h8_t8192|prefill_8x16384_h96|prefill_varlen16_h32|prefill_h1_t64]
+                  [--decode-rows R] [--state-dtype f32|bf16] [--no-e2e] [--no-cpu-baseline]
+
+``--impl reference`` times the FP64 oracle (the CPU reference of this build) on the
+host cores on a bounded sample of the same workload and prints the same JSON shape.
+Under torchrun each rank runs its own copy of the workload (weak scaling: chains are
+independent, so no collective touches the data path); rank 0 prints the line with the
+maximum time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens·heads/s (d=128) + decode rows·heads/s; % of roofline"
+PREFILL_BYTES_PER_TOKEN_HEAD = 4 * 256 + 4 + 256  # q, k, v, g_raw (BF16 x 128) + beta + out
+STATE_BYTES = 128 * 128 * 4                        # one FP32 state
+PREFILL_FLOP_PER_TOKEN_HEAD = 6 * 128 * 128 + 8 * 32 * 128
+DECODE_IO_BYTES_PER_ROW_HEAD = 4 * 256 + 4 + 256   # q, k, v, g_raw, beta, out
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--prefill", default="prefill_h8_t8192")
+    p.add_argument("--decode-rows", type=int, default=4096)
+    p.add_argument("--state-dtype", default="f32", choices=["f32", "bf16"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The maximum of ``value`` over all ranks (identity on one rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own synthetic copy of the workload."""
+    return base + 1000003 * rank
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+
+def prefill_workload(name, device, seed_offset=0):
+    import kda_synth as S
+    cfg = S.configs()[name]
+    inp = S.prefill_inputs(cfg.seqlens, cfg.num_heads, seed=rank_seed(cfg.seed, seed_offset), init_std=cfg.init_std,
+                           device=device)
+    return cfg, inp
+
+
+def decode_workload(rows, state_dtype, device, seed_offset=0):
+    import kda_synth as S
+    cfg = S.configs()["decode_h8_pool16384"]
+    seed = rank_seed(cfg.seed, seed_offset)
+    pool = S.state_pool(cfg.num_slots, cfg.num_heads, state_dtype, std=cfg.pool_std, seed=seed, device=device)
+    inp = S.decode_inputs(rows, cfg.num_heads, seed=seed, device=device)
+    inp["slot_idx"] = S.slot_indices(rows, cfg.num_slots, seed=seed, device=device)
+    return cfg, pool, inp
+
+
+def prefill_units(cfg):
+    return cfg.total_tokens * cfg.num_heads
+
+
+def prefill_bytes(cfg):
+    chains = len(cfg.seqlens) * cfg.num_heads
+    state_io = chains * STATE_BYTES * (2 if cfg.init_std is not None else 1)
+    return prefill_units(cfg) * PREFILL_BYTES_PER_TOKEN_HEAD + state_io
+
+
+def decode_bytes(rows, heads, state_dtype):
+    per_state = 128 * 128 * (4 if state_dtype == "f32" else 2)
+    return rows * heads * (2 * per_state + DECODE_IO_BYTES_PER_ROW_HEAD) + rows * 4
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+
+    import kda_recurrent_gb300 as K
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    K.load(build_if_missing=True)
+    peaks, peak_src = load_peaks()
+
+    pcfg, pin = prefill_workload(args.prefill, device, rank)
+    dcfg, pool, din = decode_workload(args.decode_rows, args.state_dtype, device, rank)
+    scale = pcfg.scale
+    out = torch.empty_like(pin["q"])
+    fin = torch.empty(len(pcfg.seqlens), pcfg.num_heads, 128, 128, dtype=torch.float32, device=device)
+    dout = torch.empty_like(din["q"])
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 512 << 20), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def prefill_call():
+        K.kda_prefill(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta"], pin["cu_seqlens"], pin["init_state"],
+                      out, fin, scale, pcfg.lower_bound, pcfg.gate_mode, stream)
+
+    def decode_call():
+        K.kda_decode(din["q"], din["k"], din["v"], din["g_raw"], din["beta"], din["slot_idx"], pool, dout, dcfg.scale,
+                     dcfg.lower_bound, dcfg.gate_mode, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill_call()
+        decode_call()
+    torch.cuda.synchronize(device)
+    st, detail = K.kda_device_status()
+    if st != K.KDA_OK:
+        raise RuntimeError(f"device status {st} ({detail}) after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.__enter__()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        prefill_call()
+        ev[s][1].record(stream)
+        decode_call()
+        ev[s][2].record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    if sampler:
+        sampler.__exit__(None, None, None)
+    p_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    d_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    p_mean = max_over_ranks(sum(p_ms) / len(p_ms), dist, device)
+    d_mean = max_over_ranks(sum(d_ms) / len(d_ms), dist, device)
+    st, detail = K.kda_device_status()
+    if st != K.KDA_OK:
+        raise RuntimeError(f"device status {st} ({detail}) after the timed region")
+
+    e2e = None if args.no_e2e else measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = cpu_baseline(pcfg, pin, dcfg, din, pool)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    p_units = prefill_units(pcfg) * world
+    d_units = args.decode_rows * dcfg.num_heads * world
+    p_rate = p_units / (p_mean * 1e-3)
+    d_rate = d_units / (d_mean * 1e-3)
+    p_bytes = prefill_bytes(pcfg)
+    d_bytes = decode_bytes(args.decode_rows, dcfg.num_heads, args.state_dtype)
+    p_gbs = p_bytes / (p_mean * 1e-3) / 1e9
+    d_gbs = d_bytes / (d_mean * 1e-3) / 1e9
+    p_tflops = prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD / (p_mean * 1e-3) / 1e12
+    traffic = load_traffic()
+    prefill_roof = {"bound": "hbm", "achieved": round(p_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(p_gbs / peaks["hbm_gbs"], 5), "traffic": traffic.get("kda_prefill_kernel"),
+                    "kernel": "kda_prefill_kernel", "peak_source": peak_src,
+                    "algorithmic_bytes_per_launch": p_bytes,
+                    "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                               "frac": round(p_tflops / peaks["bf16_tflops"], 5),
+                               "flop_per_launch": prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD}}
+    decode_roof = {"bound": "hbm", "achieved": round(d_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": round(d_gbs / peaks["hbm_gbs"], 5), "traffic": traffic.get("kda_decode_kernel"),
+                   "kernel": "kda_decode_kernel", "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes}
+    dominant = prefill_roof if p_mean >= d_mean else decode_roof
+    line = {
+        "metric": METRIC, "value": round(p_rate, 1), "unit": "tokens*heads/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(p_mean + d_mean, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool16384",
+                   "prefill": {"seqlens": pcfg.seqlens if len(pcfg.seqlens) <= 16 else f"{len(pcfg.seqlens)} seqs",
+                               "heads": pcfg.num_heads, "gate": pcfg.gate_mode, "lower_bound": pcfg.lower_bound,
+                               "init_state": pcfg.init_std is not None},
+                   "decode": {"rows": args.decode_rows, "heads": dcfg.num_heads, "pool_slots": dcfg.num_slots,
+                              "state_dtype": args.state_dtype},
+                   "precision": "bf16 operands, tf32 state update, fp32 state and accumulation",
+                   "l2": f"flushed between steps ({flush.numel() >> 20} MiB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "prefill": {"value": round(p_rate, 1), "unit": "tokens*heads/s", "ms": round(p_mean, 4),
+                    "us_per_chunk_per_chain": round(p_mean * 1e3 / math.ceil(max(pcfg.seqlens) / 32), 4)},
+        "decode": {"value": round(d_rate, 1), "unit": "rows*heads/s", "ms": round(d_mean, 4), "roofline": decode_roof},
+        "roofline": dominant,
+        "roofline_prefill": prefill_roof,
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if sampler:
+        line["clocks"] = sampler.summary()
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist):
+    """Same metric through the C ABI from pinned host buffers: H2D of the step's inputs,
+    the two calls, D2H of the outputs (prefill out + final state, decode out)."""
+    import torch
+    host_p = {k: (v.to("cpu").pin_memory() if v is not None else None) for k, v in pin.items()}
+    host_d = {k: v.to("cpu").pin_memory() for k, v in din.items()}
+    dev_p = {k: (torch.empty_like(v, device=device) if v is not None else None) for k, v in host_p.items()}
+    dev_d = {k: torch.empty_like(v, device=device) for k, v in host_d.items()}
+    out = torch.empty_like(dev_p["q"])
+    fin = torch.empty(len(pcfg.seqlens), pcfg.num_heads, 128, 128, dtype=torch.float32, device=device)
+    dout = torch.empty_like(dev_d["q"])
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h_dout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_p.values() if v is not None)
+    h2d_d = sum(v.numel() * v.element_size() for v in host_d.values())
+    d2h = h_out.numel() * 2 + h_fin.numel() * 4
+    d2h_d = h_dout.numel() * 2
+
+    def step():
+        for k2, v in host_p.items():
+            if v is not None:
+                dev_p[k2].copy_(v, non_blocking=True)
+        K.kda_prefill(dev_p["q"], dev_p["k"], dev_p["v"], dev_p["g_raw"], dev_p["beta"], dev_p["cu_seqlens"],
+                      dev_p["init_state"], out, fin, pcfg.scale, pcfg.lower_bound, pcfg.gate_mode, stream)
+        h_out.copy_(out, non_blocking=True)
+        h_fin.copy_(fin, non_blocking=True)
+
+    def dstep():
+        for k2, v in host_d.items():
+            dev_d[k2].copy_(v, non_blocking=True)
+        K.kda_decode(dev_d["q"], dev_d["k"], dev_d["v"], dev_d["g_raw"], dev_d["beta"], dev_d["slot_idx"], pool, dout,
+                     dcfg.scale, dcfg.lower_bound, dcfg.gate_mode, stream)
+        h_dout.copy_(dout, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        step()
+        dstep()
+    torch.cuda.synchronize(device)
+    steps = max(3, args.steps // 2)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for s in range(steps):
+        ev[s][0].record(stream)
+        step()
+        ev[s][1].record(stream)
+        dstep()
+        ev[s][2].record(stream)
+    torch.cuda.synchronize(device)
+    p_ms = max_over_ranks(sum(ev[s][0].elapsed_time(ev[s][1]) for s in range(steps)) / steps, dist, device)
+    d_ms = max_over_ranks(sum(ev[s][1].elapsed_time(ev[s][2]) for s in range(steps)) / steps, dist, device)
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": round(prefill_units(pcfg) * world / (p_ms * 1e-3), 1), "unit": "tokens*heads/s",
+            "h2d_bytes_per_step": int(h2d + h2d_d), "d2h_bytes_per_step": int(d2h + d2h_d),
+            "prefill_ms": round(p_ms, 4), "decode_ms": round(d_ms, 4),
+            "decode_value": round(args.decode_rows * dcfg.num_heads * world / (d_ms * 1e-3), 1),
+            "decode_unit": "rows*heads/s"}
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of each kernel from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: v.get("dram_bytes_per_launch") for k, v in d.items() if v.get("current", False)}
+    except (OSError, ValueError):
+        return {}
+
+
+# ------------------------------------------------------------------ oracle timing (CPU baseline)
+
+def oracle_sample(pcfg, pin, dcfg, din, pool, budget_s=20.0):
+    """Times the FP64 oracle on the host cores on bounded samples of the workload."""
+    import torch
+
+    import oracle
+    cpu_p = {k: (v.to("cpu") if v is not None else None) for k, v in pin.items()}
+    H = pcfg.num_heads
+    cu = cpu_p["cu_seqlens"].tolist()
+    # prefill sample: every head of the first sequence, first `toks` tokens (grown to fill the budget)
+    toks = min(512, cu[1] - cu[0])
+    res = {}
+    while True:
+        sub = {k: (cpu_p[k][:toks] if k in ("q", "k", "v", "g_raw", "beta") else None) for k in cpu_p}
+        init = None if cpu_p["init_state"] is None else cpu_p["init_state"][:1]
+        t0 = time.perf_counter()
+        _, _, threads = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g_raw"], sub["beta"],
+                                       torch.tensor([0, toks], dtype=torch.int32), init, scale=pcfg.scale,
+                                       lower_bound=pcfg.lower_bound, gate_mode=pcfg.gate_mode)
+        dt = time.perf_counter() - t0
+        res["prefill"] = (toks * H / dt, threads, f"sequence 0, first {toks} tokens, all {H} heads")
+        if dt > budget_s / 4 or toks >= cu[1] - cu[0]:
+            break
+        toks = min(cu[1] - cu[0], toks * 4)
+    rows = min(din["q"].shape[0], 1024)
+    gathered = pool[din["slot_idx"][:rows].long()].to("cpu")
+    t0 = time.perf_counter()
+    _, _, threads_d = oracle.decode(din["q"][:rows].cpu(), din["k"][:rows].cpu(), din["v"][:rows].cpu(),
+                                    din["g_raw"][:rows].cpu(), din["beta"][:rows].cpu(), gathered, scale=dcfg.scale,
+                                    lower_bound=dcfg.lower_bound, gate_mode=dcfg.gate_mode)
+    dt = time.perf_counter() - t0
+    res["decode"] = (rows * dcfg.num_heads / dt, threads_d, f"first {rows} rows, all {dcfg.num_heads} heads")
+    return res
+
+
+def cpu_baseline(pcfg, pin, dcfg, din, pool):
+    res = oracle_sample(pcfg, pin, dcfg, din, pool)
+    p_rate, p_threads, p_sample = res["prefill"]
+    d_rate, d_threads, d_sample = res["decode"]
+    return {"value": round(p_rate, 2), "unit": "tokens*heads/s", "cores": p_threads, "kind": "oracle",
+            "sample": f"prefill: {p_sample}", "host_cores": os.cpu_count(),
+            "decode": {"value": round(d_rate, 2), "unit": "rows*heads/s", "cores": d_threads, "sample": d_sample}}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return None
+    import torch
+    pcfg, pin = prefill_workload(args.prefill, "cpu", 0)
+    dcfg = __import__("kda_synth").configs()["decode_h8_pool16384"]
+    import kda_synth as S
+    din = S.decode_inputs(min(args.decode_rows, 1024), dcfg.num_heads, seed=dcfg.seed)
+    din["slot_idx"] = torch.arange(din["q"].shape[0], dtype=torch.int32)
+    pool = S.state_pool(din["q"].shape[0], dcfg.num_heads, args.state_dtype, std=dcfg.pool_std, seed=dcfg.seed)
+    budget = max(4.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(pcfg, pin, dcfg, din, pool, budget_s=budget)
+    p_rates, d_rates = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = oracle_sample(pcfg, pin, dcfg, din, pool, budget_s=budget)
+        p_rates.append(r["prefill"][0])
+        d_rates.append(r["decode"][0])
+    wall = time.perf_counter() - t0
+    p_rate = statistics.median(p_rates)
+    return {"impl": "reference", "metric": METRIC, "value": round(p_rate, 2), "unit": "tokens*heads/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall * 1e3 / max(1, args.steps), 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool16384",
+                       "note": "FP64 CPU oracle on bounded samples of the workload"},
+            "decode": {"value": round(statistics.median(d_rates), 2), "unit": "rows*heads/s"},
+            "cpu_baseline": {"value": round(p_rate, 2), "unit": "tokens*heads/s", "cores": r["prefill"][1],
+                             "kind": "oracle", "sample": f"prefill: {r['prefill'][2]}; decode: {r['decode'][2]}"},
+            "e2e": {"value": round(p_rate, 2), "unit": "tokens*heads/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

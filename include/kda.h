@@ -1,0 +1,159 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention hot path.
+ *
+ * KDA is a gated delta rule with a per-channel log decay. Per head it carries
+ * an FP32 state S[dk = 128][dv = 128] and, token by token,
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * Two entry points run it on the GPU:
+ *   kda_prefill -- varlen sequences, computed chunk by chunk (32 tokens) in the
+ *                  chunked form of "FlashInfer PR #4262: CAKE KDA Prefill
+ *                  Highlights", section 2 (gate prefix sums, causal Mqk, 32 x 32
+ *                  lower-triangular inverse, state decay and projection,
+ *                  residual/beta transform, fused state + output update, output
+ *                  store);
+ *   kda_decode  -- one token per row against a slot-indexed state pool, updated
+ *                  in place (FlashInfer PR #5551, "Kimi K3 TP12 H=8 fused KDA
+ *                  decode": state pool + slot indices, lower-bound or softplus
+ *                  gate, caller-owned outputs).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless stated, owned by the caller. The
+ *     library allocates nothing per call; its only global memory is a small
+ *     device status word in the library image (see kda_device_status).
+ *   - Every tensor is dense and row-major in the layout given. BF16 means IEEE
+ *     bfloat16 bit patterns (uint16 storage). Tensor base addresses must be
+ *     16-byte aligned (beta, cu_seqlens and slot_idx: 4-byte), else
+ *     KDA_ERR_MISALIGNED.
+ *   - The head dimension is fixed: dk = dv = KDA_HEAD_DIM = 128.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream),
+ *     never synchronise, and return a kda_status. Argument errors are found on
+ *     the host before anything is launched. A failed launch returns
+ *     KDA_ERR_CUDA. Errors in device-resident index data are recorded in the
+ *     device status word, never by a trap.
+ *   - Gate modes: g is a per-channel natural-log decay computed from the raw
+ *     gate a (g_raw) as
+ *       KDA_GATE_LOWER_BOUND  g = lower_bound * sigmoid(a)   (lower_bound <= 0;
+ *                             the "bounded lb" gate of PR #5551/#5565)
+ *       KDA_GATE_SOFTPLUS     g = -softplus(a)               (the unbounded
+ *                             "Kimi-Linear softplus" gate of PR #5565)
+ *       KDA_GATE_LOG_DECAY    g = a                          (a <= 0 supplied
+ *                             directly; positive values are not checked and
+ *                             make the state grow)
+ *   - beta is post-sigmoid, FP32, in [0, 1].
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+/* Same type as cudaStream_t; declared here so callers need no CUDA header. */
+typedef struct CUstream_st *kda_stream_t;
+
+#define KDA_HEAD_DIM 128
+#define KDA_CHUNK 32
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,    /* bad size, NULL pointer, bad mode or scalar        */
+    KDA_ERR_UNSUPPORTED = -2,    /* a valid request this build does not run           */
+    KDA_ERR_MISALIGNED = -3,     /* a pointer breaks the alignment rule above         */
+    KDA_ERR_CUDA = -4,           /* a CUDA runtime call or launch failed              */
+    KDA_ERR_DEVICE_TIMEOUT = -5, /* (device status) a bounded device wait gave up     */
+    KDA_ERR_DEVICE_INPUT = -6    /* (device status) bad device-resident index data    */
+} kda_status;
+
+typedef enum {
+    KDA_GATE_LOWER_BOUND = 0,
+    KDA_GATE_SOFTPLUS = 1,
+    KDA_GATE_LOG_DECAY = 2
+} kda_gate_mode;
+
+typedef enum { KDA_STATE_F32 = 0, KDA_STATE_BF16 = 1 } kda_state_dtype;
+
+/*
+ * kda_prefill -- chunk-32 varlen prefill.
+ *   q, k, g_raw  BF16 [total_tokens, num_heads, 128]   (q, k as given; no normalisation)
+ *   v            BF16 [total_tokens, num_heads, 128]
+ *   beta         FP32 [total_tokens, num_heads]
+ *   cu_seqlens   int32 [num_seqs + 1], device; cu[0] = 0, non-decreasing,
+ *                cu[num_seqs] = total_tokens. Sequence n is tokens
+ *                [cu[n], cu[n+1]). Violations cannot fault: every index is
+ *                clamped into range and KDA_ERR_DEVICE_INPUT is recorded.
+ *   init_state   FP32 [num_seqs, num_heads, 128(dk), 128(dv)], or NULL for zeros
+ *   out          BF16 [total_tokens, num_heads, 128], written for every token
+ *   final_state  FP32 [num_seqs, num_heads, 128, 128], or NULL to skip. May equal
+ *                init_state (in-place carry: each chain reads its initial state
+ *                before it writes its final state). A zero-length sequence copies
+ *                its initial state (or zeros) to final_state.
+ *   scale        multiplies every output (typically 1/sqrt(128))
+ *   lower_bound  used by KDA_GATE_LOWER_BOUND only; must be finite and <= 0
+ *   gate_mode    a kda_gate_mode
+ * q/k/v/g_raw/beta must not overlap out or final_state. num_seqs >= 0,
+ * total_tokens >= 0, num_heads >= 1. num_seqs == 0 is a no-op.
+ * Work: one thread block per (sequence, head) chain walking its chunks in order;
+ * the FP32 state stays on chip for the whole sequence.
+ */
+KDA_API int kda_prefill(const void *q, const void *k, const void *v, const void *g_raw,
+                const float *beta, const int32_t *cu_seqlens, const float *init_state,
+                void *out, float *final_state, int32_t num_seqs, int32_t total_tokens,
+                int32_t num_heads, float scale, float lower_bound, int32_t gate_mode,
+                kda_stream_t stream);
+
+/*
+ * kda_decode -- one token per row (T = 1) against a slot-indexed state pool.
+ *   q, k, g_raw  BF16 [rows, num_heads, 128]
+ *   v            BF16 [rows, num_heads, 128]
+ *   beta         FP32 [rows, num_heads]
+ *   slot_idx     int32 [rows], device. Row r updates pool slot slot_idx[r] for every
+ *                head. Slots must be unique (duplicates race; not detected). A
+ *                negative slot marks a padding row: its outputs are written as
+ *                zeros and no state is touched. A slot >= num_slots is treated as
+ *                padding and recorded as KDA_ERR_DEVICE_INPUT.
+ *   state_pool   [num_slots, num_heads, 128(dk), 128(dv)] of FP32 or BF16
+ *                (state_dtype), updated in place. Offsets are 64-bit, so pools of
+ *                2^31 elements and more are fine. Slots not named in slot_idx are
+ *                never read or written. BF16 states are computed in FP32 and
+ *                stored rounded to nearest even.
+ *   out          BF16 [rows, num_heads, 128]
+ *   scale, lower_bound, gate_mode as for kda_prefill.
+ * rows >= 0 (0 is a no-op), num_heads >= 1, num_slots >= 1.
+ */
+KDA_API int kda_decode(const void *q, const void *k, const void *v, const void *g_raw,
+               const float *beta, const int32_t *slot_idx, void *state_pool, int64_t num_slots,
+               int32_t state_dtype, void *out, int32_t rows, int32_t num_heads, float scale,
+               float lower_bound, int32_t gate_mode, kda_stream_t stream);
+
+/* A static, human-readable name for a kda_status value. Never NULL. */
+KDA_API const char *kda_status_string(int status);
+
+/*
+ * kda_device_status -- reads and clears the device status word of the current
+ * device. Synchronises `stream` (the only entry point that does). Returns KDA_OK,
+ * KDA_ERR_DEVICE_INPUT or KDA_ERR_DEVICE_TIMEOUT (the first error recorded since
+ * the last read), or KDA_ERR_CUDA if the read itself failed. If `detail` is not
+ * NULL it receives a code-specific detail (for KDA_ERR_DEVICE_INPUT: the
+ * offending sequence or row index).
+ */
+KDA_API int kda_device_status(kda_stream_t stream, int32_t *detail);
+
+/* ABI version of this header: (major << 16) | minor. */
+KDA_API int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,184 @@
+"""GB300 (sm_103a) Kimi Delta Attention hot path: Python binding of the C ABI in ``include/kda.h``.
+
+Every step of the computation runs in the CUDA library ``_build/libkda_gb300.so``;
+this module only marshals arguments (dtype / shape / device checks, raw pointers,
+the current CUDA stream). If the library is missing it raises -- there is no other
+implementation behind these calls.
+
+Low-level calls mirror the C names and take caller-owned torch tensors:
+    kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, scale,
+                lower_bound, gate_mode, stream=None)
+    kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound,
+               gate_mode, stream=None)
+    kda_status_string(status), kda_device_status(stream=None)
+Convenience wrappers ``prefill`` / ``decode`` allocate the outputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_MISALIGNED = -3
+KDA_ERR_CUDA = -4
+KDA_ERR_DEVICE_TIMEOUT = -5
+KDA_ERR_DEVICE_INPUT = -6
+
+GATE_MODES = {"lower_bound": 0, "softplus": 1, "log_decay": 2}
+STATE_DTYPES = {"f32": 0, "bf16": 1}
+HEAD_DIM = 128
+CHUNK = 32
+
+EXPORTED_SYMBOLS = ("kda_prefill", "kda_decode", "kda_status_string", "kda_device_status", "kda_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {kda_status_string(status)} ({status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load the CUDA library (building it first only if asked). Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise RuntimeError(f"KDA CUDA library not built: {path} (run kda_recurrent_gb300.build.build())")
+                _build.build()
+            lib = ctypes.CDLL(path)
+            vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+            lib.kda_prefill.restype = ctypes.c_int
+            lib.kda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
+            lib.kda_decode.restype = ctypes.c_int
+            lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, vp]
+            lib.kda_status_string.restype = ctypes.c_char_p
+            lib.kda_status_string.argtypes = [ctypes.c_int]
+            lib.kda_device_status.restype = ctypes.c_int
+            lib.kda_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+            lib.kda_abi_version.restype = ctypes.c_int
+            lib.kda_abi_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _mode(gate_mode) -> int:
+    return GATE_MODES[gate_mode] if isinstance(gate_mode, str) else int(gate_mode)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, shape, device):
+    import torch
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    del torch
+
+
+def kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, scale, lower_bound=0.0,
+                gate_mode="lower_bound", stream=None):
+    """Varlen chunk-32 prefill into caller-owned ``out`` / ``final_state`` (see include/kda.h)."""
+    import torch
+    T, H, d = q.shape
+    N = cu_seqlens.shape[0] - 1
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("out", out)):
+        _check(t, name, torch.bfloat16, (T, H, d), dev)
+    _check(beta, "beta", torch.float32, (T, H), dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    for name, t in (("init_state", init_state), ("final_state", final_state)):
+        if t is not None:
+            _check(t, name, torch.float32, (N, H, d, d), dev)
+    st = load().kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
+                            _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
+                            float(lower_bound), _mode(gate_mode), _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill")
+
+
+def kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound=0.0,
+               gate_mode="lower_bound", stream=None):
+    """T = 1 decode of ``rows`` tokens against ``state_pool`` (updated in place)."""
+    import torch
+    R, H, d = q.shape
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("out", out)):
+        _check(t, name, torch.bfloat16, (R, H, d), dev)
+    _check(beta, "beta", torch.float32, (R, H), dev)
+    _check(slot_idx, "slot_idx", torch.int32, (R,), dev)
+    if state_pool.dtype == torch.float32:
+        sdt = STATE_DTYPES["f32"]
+    elif state_pool.dtype == torch.bfloat16:
+        sdt = STATE_DTYPES["bf16"]
+    else:
+        raise TypeError("state_pool must be float32 or bfloat16")
+    _check(state_pool, "state_pool", state_pool.dtype, (state_pool.shape[0], H, d, d), dev)
+    st = load().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(slot_idx), _ptr(state_pool),
+                           int(state_pool.shape[0]), sdt, _ptr(out), R, H, float(scale), float(lower_bound),
+                           _mode(gate_mode), _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode")
+
+
+def kda_device_status(stream=None):
+    """(status, detail): reads and clears the device status word (synchronises the stream)."""
+    import torch
+    detail = ctypes.c_int32(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = load().kda_device_status(_stream_handle(stream, dev), ctypes.byref(detail))
+    return st, detail.value
+
+
+def prefill(q, k, v, g_raw, beta, cu_seqlens, init_state=None, *, scale, lower_bound=0.0,
+            gate_mode="lower_bound", want_final=True, stream=None):
+    """Allocates ``out`` (and ``final_state``) and runs ``kda_prefill``; returns (out, final_state)."""
+    import torch
+    T, H, d = q.shape
+    N = cu_seqlens.shape[0] - 1
+    out = torch.empty_like(q)
+    final = torch.empty(N, H, d, d, dtype=torch.float32, device=q.device) if want_final else None
+    kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final, scale, lower_bound, gate_mode, stream)
+    return out, final
+
+
+def decode(q, k, v, g_raw, beta, slot_idx, state_pool, *, scale, lower_bound=0.0, gate_mode="lower_bound",
+           stream=None):
+    """Allocates ``out`` and runs ``kda_decode`` (pool updated in place); returns out."""
+    import torch
+    out = torch.empty_like(q)
+    kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, stream)
+    del torch
+    return out

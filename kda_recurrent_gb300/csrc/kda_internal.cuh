@@ -1,0 +1,58 @@
+// Internal declarations shared by the translation units of the KDA library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kHeadDim = KDA_HEAD_DIM;  // dk = dv = 128
+constexpr int kChunk = KDA_CHUNK;       // prefill chunk length
+
+// Device status word: [0] = first kda_status error code recorded, [1] = its detail.
+struct DeviceStatus {
+    int32_t code;
+    int32_t detail;
+};
+
+// Records `code` (if no earlier error is pending) and its detail. Device side.
+__device__ __forceinline__ void report_error(DeviceStatus *st, int32_t code, int32_t detail) {
+    if (st != nullptr && atomicCAS(&st->code, 0, code) == 0) {
+        st->detail = detail;
+    }
+}
+
+// Address of the device status word of the current device (set up on first use).
+cudaError_t device_status_ptr(DeviceStatus **out);
+
+struct DecodeArgs {
+    const __nv_bfloat16 *q, *k, *v, *g_raw;
+    const float *beta;
+    const int32_t *slot_idx;
+    void *state_pool;
+    int64_t num_slots;
+    __nv_bfloat16 *out;
+    int32_t rows, num_heads, gate_mode, state_dtype;
+    float scale, lower_bound;
+    DeviceStatus *status;
+};
+
+struct PrefillArgs {
+    const __nv_bfloat16 *q, *k, *v, *g_raw;
+    const float *beta;
+    const int32_t *cu_seqlens;
+    const float *init_state;
+    __nv_bfloat16 *out;
+    float *final_state;
+    int32_t num_seqs, total_tokens, num_heads, gate_mode;
+    float scale, lower_bound;
+    DeviceStatus *status;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, exports
+every entry point include/kda.h declares, and rejects bad arguments before any CUDA call.
+
+Pointer arguments here are plain integers that are never dereferenced: every case
+below fails validation on the host, which happens before the library touches the
+device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import kda_recurrent_gb300 as K
+from kda_recurrent_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return K.load()
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_bound_entry_points():
+    assert declared_entry_points() == sorted(K.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.kda_abi_version() >> 16 == 1
+    for code in (0, -1, -2, -3, -4, -5, -6, 99):
+        assert isinstance(K.kda_status_string(code), str) and K.kda_status_string(code)
+    assert K.kda_status_string(K.KDA_ERR_MISALIGNED) == "misaligned pointer"
+
+
+A16 = 0x10000  # a 16-byte-aligned fake address (never dereferenced)
+
+
+def prefill_call(lib, **over):
+    args = dict(q=A16, k=A16, v=A16, g=A16, beta=A16, cu=A16, init=None, out=A16, fin=None, N=1, T=32, H=2,
+                scale=0.1, lb=-5.0, mode=0)
+    args.update(over)
+    return lib.kda_prefill(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"], args["init"],
+                           args["out"], args["fin"], args["N"], args["T"], args["H"], args["scale"], args["lb"],
+                           args["mode"], None)
+
+
+def decode_call(lib, **over):
+    args = dict(q=A16, k=A16, v=A16, g=A16, beta=A16, slots=A16, pool=A16, S=16, dt=0, out=A16, R=4, H=2,
+                scale=0.1, lb=-5.0, mode=0)
+    args.update(over)
+    return lib.kda_decode(args["q"], args["k"], args["v"], args["g"], args["beta"], args["slots"], args["pool"],
+                          args["S"], args["dt"], args["out"], args["R"], args["H"], args["scale"], args["lb"],
+                          args["mode"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(H=0), K.KDA_ERR_INVALID_ARG),
+    (dict(N=-1), K.KDA_ERR_INVALID_ARG),
+    (dict(T=-5), K.KDA_ERR_INVALID_ARG),
+    (dict(mode=3), K.KDA_ERR_INVALID_ARG),
+    (dict(lb=1.0), K.KDA_ERR_INVALID_ARG),
+    (dict(lb=float("nan")), K.KDA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), K.KDA_ERR_INVALID_ARG),
+    (dict(q=None), K.KDA_ERR_INVALID_ARG),
+    (dict(out=None), K.KDA_ERR_INVALID_ARG),
+    (dict(cu=None), K.KDA_ERR_INVALID_ARG),
+    (dict(N=0, T=5), K.KDA_ERR_INVALID_ARG),
+    (dict(q=A16 + 8), K.KDA_ERR_MISALIGNED),
+    (dict(out=A16 + 2), K.KDA_ERR_MISALIGNED),
+    (dict(fin=A16 + 4), K.KDA_ERR_MISALIGNED),
+    (dict(beta=A16 + 2), K.KDA_ERR_MISALIGNED),
+    (dict(N=0, T=0), K.KDA_OK),
+    (dict(T=0, fin=None), K.KDA_OK),
+])
+def test_prefill_rejects_bad_arguments_on_host(lib, over, expect):
+    assert prefill_call(lib, **over) == expect
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(H=0), K.KDA_ERR_INVALID_ARG),
+    (dict(R=-1), K.KDA_ERR_INVALID_ARG),
+    (dict(S=0), K.KDA_ERR_INVALID_ARG),
+    (dict(dt=2), K.KDA_ERR_INVALID_ARG),
+    (dict(mode=-1), K.KDA_ERR_INVALID_ARG),
+    (dict(lb=0.5), K.KDA_ERR_INVALID_ARG),
+    (dict(pool=None), K.KDA_ERR_INVALID_ARG),
+    (dict(slots=None), K.KDA_ERR_INVALID_ARG),
+    (dict(pool=A16 + 4), K.KDA_ERR_MISALIGNED),
+    (dict(v=A16 + 1), K.KDA_ERR_MISALIGNED),
+    (dict(slots=A16 + 2), K.KDA_ERR_MISALIGNED),
+    (dict(R=0), K.KDA_OK),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, over, expect):
+    assert decode_call(lib, **over) == expect
+
+
+def test_binding_checks_dtypes_and_shapes_before_calling(lib):
+    q = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    beta = torch.zeros(4, 2)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(TypeError):
+        K.kda_prefill(q.float(), q, q, q, beta, cu, None, q, None, 0.1)
+    with pytest.raises(ValueError):
+        K.kda_prefill(q, q, q, q, beta[:3], cu, None, q, None, 0.1)
+    with pytest.raises(TypeError):
+        K.kda_decode(q, q, q, q, beta, torch.zeros(4, dtype=torch.int64), torch.zeros(8, 2, 128, 128), q, 0.1)
+
+
+def test_product_path_has_no_fallback(monkeypatch, tmp_path):
+    """Without the built library the binding raises; nothing else computes."""
+    monkeypatch.setattr(kbuild, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(K, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        K.load()
