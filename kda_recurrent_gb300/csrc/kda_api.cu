@@ -98,7 +98,7 @@ int kda_prefill(const void *q, const void *k, const void *v, const void *g_raw, 
     a.lower_bound = lower_bound;
     cudaError_t e = device_status_ptr(&a.status);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    return from_cuda(launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int kda_decode(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,

@@ -54,5 +54,6 @@ struct PrefillArgs {
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 
 }  // namespace kda

@@ -1,0 +1,739 @@
+// Chunk-32 varlen KDA prefill, tcgen05 / TMEM version (sm_103a).
+//
+// Same chunk algebra as "FlashInfer PR #4262: CAKE KDA Prefill Highlights", section 2, in
+// the reassociated form (Wk = T'Kbar, Wv = T'V, Q' = Qbar - Mqk Wk, Ov = Mqk Wv):
+//     U = Wv - Wk S,   O = Ov + Q' S,   S_new = Diag(2^G_last) S + Kr^T U.
+//
+// As on the page, the FP32 recurrent state stays in tensor memory for the whole sequence
+// and the state-sized products run on tcgen05; unlike the page, the accumulator is
+// preloaded so that the projection itself produces U and O:
+//     D1^T[dv, 0:32]  = Wv^T,   D1^T[dv, 32:64] = Ov^T         (producer tcgen05.st)
+//     D1^T += S^T [-Wk; Q']^T      M128 N64 K128, kind::tf32, A = S^T read from TMEM
+//     S_nxt = S_cur Diag(2^G_last)                              (state warps, TMEM -> TMEM)
+//     S_nxt^T += U^T Kr            M128 N128 K32, kind::tf32, A = U^T read from TMEM
+// so nothing on the serial chain passes through registers except the decay. The state
+// is ping-ponged between two TMEM buffers so that the decay runs while the projection
+// reads the previous buffer.
+//
+// Warp roles (one CTA per (sequence, head) chain, 12 warps):
+//   warps 0-7  producers: raw loads (cp.async), gate and decay products, pair products and
+//              the 32 x 32 inverse (mma.sync, FP32), Wk/Wv/Q'/Ov (mma.sync), then the chunk
+//              operands into a two-deep SMEM stage ring and Wv/Ov into TMEM;
+//   warps 8-11 state warps (one per TMEM lane quadrant): initial/final state, the decay,
+//              the output read-out and store; lane 0 of warp 8 issues the MMAs.
+// Exponent range: per 16-token half, factors are anchored at the half's 8th token, built
+// as running products of the per-token decays (no per-element exp of a prefix); the
+// off-diagonal block factors through the half boundary (both factors <= 1).
+// All mbarrier waits are bounded; on expiry the kernel records KDA_ERR_DEVICE_TIMEOUT,
+// drains, frees its tensor memory and returns.
+#include "kda_internal.cuh"
+#include "kda_mma.cuh"
+#include "kda_tc.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kProducerWarps = 8;
+constexpr int kStateWarps = 4;
+constexpr int kFirstStateWarp = kProducerWarps;
+constexpr int kThreadsTc = (kProducerWarps + kStateWarps) * 32;
+constexpr int kProdThreads = kProducerWarps * 32;
+constexpr int kStateThreads = kStateWarps * 32;
+constexpr int kBarProd = 1;   // named barrier of the producer warps
+constexpr int kBarState = 2;  // named barrier of the state warps
+
+constexpr int kRowB = 136;  // padded bf16 row stride (ldmatrix operands)
+constexpr int kRowF = 132;  // padded fp32 row stride
+constexpr int kSq = 36;     // fp32 32 x 32 tiles
+constexpr int kSmall = 20;  // fp32 16 x 16 tiles
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- shared-memory map (bytes)
+constexpr int kRawQ = 0;                          // bf16 [32][128]
+constexpr int kRawK = kRawQ + 8192;
+constexpr int kRawA = kRawK + 8192;
+constexpr int kRawV = kRawA + 8192;               // bf16 [32][136]
+constexpr int kRawBeta = kRawV + 32 * kRowB * 2;  // fp32 [32]
+constexpr int kStage0 = kRawBeta + 128;
+constexpr int kStW = 0;                           // tf32, K-major core matrices, [64 tok][128 dk]
+constexpr int kStKr = 32768;                      // tf32, K-major core matrices, [128 dk][32 tok]
+constexpr int kStDec = 49152;                     // fp32 [128]
+constexpr int kStageBytes = kStDec + 512;
+constexpr int kPair = kStage0 + 2 * kStageBytes;  // 3 x [48][136] bf16
+constexpr int kPairQ = kPair;
+constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
+constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
+constexpr int kPairEnd = kPairKR + 48 * kRowB * 2;
+constexpr int kWvS = kPair;                       // fp32 [32][132], aliases the dead pair operands
+constexpr int kOvS = kWvS + 32 * kRowF * 4;
+constexpr int kKbar = kPairEnd;                   // bf16 [32][136]
+constexpr int kQbar = kKbar + 32 * kRowB * 2;     // bf16 [32][136]
+constexpr int kWkB = kQbar + 32 * kRowB * 2;      // bf16 [32][136]
+constexpr int kAm = kWkB + 32 * kRowB * 2;        // fp32 [32][36]: Diag(beta) A
+constexpr int kMq = kAm + 32 * kSq * 4;           // fp32 [32][36]: Mqk
+constexpr int kTp = kMq + 32 * kSq * 4;           // fp32 [32][36]: T'
+constexpr int kT22 = kTp + 32 * kSq * 4;          // fp32 [16][20]
+constexpr int kXm = kT22 + 16 * kSmall * 4;       // fp32 [16][20]
+constexpr int kHalf = kXm + 16 * kSmall * 4;      // fp32 [2][128]
+constexpr int kOst = kHalf + 2 * 128 * 4;         // bf16 [32][136]: output staging
+constexpr int kBars = kOst + 32 * kRowB * 2;
+constexpr int kSmemTc = kBars + 128;
+static_assert(kOvS + 32 * kRowF * 4 <= kPairEnd, "Wv/Ov staging fits in the pair region");
+static_assert(kStage0 % 128 == 0 && kStageBytes % 128 == 0, "stage alignment");
+static_assert(kSmemTc <= 227 * 1024, "one CTA per SM");
+
+// ---- tensor-memory map (columns; 512 allocated)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;     // S^T ping-pong: [0,128) and [128,256)
+constexpr uint32_t kColD1 = 256;  // D1 double buffer: [256,320) and [320,384)
+
+constexpr uint32_t kIdescG1 = instr_desc(2, 128, 64);   // tf32, M128 N64
+constexpr uint32_t kIdescG2 = instr_desc(2, 128, 128);  // tf32, M128 N128
+
+struct Bars {
+    uint64_t prep[2];    // producers -> state warps: stage s filled (count kProdThreads)
+    uint64_t g1;         // projection MMA complete (tcgen05.commit)
+    uint64_t g2;         // state update MMA complete (tcgen05.commit)
+    uint64_t g2s[2];     // state update of a chunk on stage s complete (tcgen05.commit)
+    uint64_t oread[2];   // D1 buffer b read out by the state warps (count kStateThreads)
+    uint32_t tmem_base;
+    int32_t abort;
+};
+static_assert(sizeof(Bars) <= 128, "barrier block");
+
+__device__ __forceinline__ void bar_named(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Bounded wait; on expiry records a timeout and raises the CTA's abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Bars *B, DeviceStatus *st) {
+    if (mbar_wait(bar, parity)) return true;
+    B->abort = 1;
+    report_error(st, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+    return false;
+}
+
+__device__ __forceinline__ float bfv(const uint8_t *base, int elem) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[elem]);
+}
+
+__device__ __forceinline__ void st_bf16(uint8_t *base, int elem, float x) {
+    reinterpret_cast<__nv_bfloat16 *>(base)[elem] = __float2bfloat16_rn(x);
+}
+
+// Byte offset of element (row, col) of a K-major tf32 operand tile made of 8-row x
+// 16-byte core matrices; `sbo` = bytes per 8-row group (rows are N, cols are K).
+__device__ __forceinline__ int core_off_tf32(int row, int col, int sbo) {
+    return (row >> 3) * sbo + (col >> 2) * 128 + (row & 7) * 16 + (col & 3) * 4;
+}
+
+__device__ __forceinline__ float gate_decay_pair(float av, int mode, float lower_bound, float &dinv) {
+    // returns d = exp(g) and sets dinv = exp(-g)
+    if (mode == KDA_GATE_LOWER_BOUND) {
+        const float s = __fdividef(1.0f, 1.0f + exp2f(-av * kLog2e));
+        const float g2 = lower_bound * s * kLog2e;
+        dinv = exp2f(-g2);
+        return exp2f(g2);
+    }
+    if (mode == KDA_GATE_SOFTPLUS) {
+        // exp(-softplus(a)) = 1 / (1 + e^a)
+        const float e = exp2f(av * kLog2e);
+        dinv = 1.0f + e;
+        return __fdividef(1.0f, dinv);
+    }
+    dinv = exp2f(-av * kLog2e);
+    return exp2f(av * kLog2e);
+}
+
+// Producer-side raw loads of one chunk: q, k, a rows (unpadded) or v rows (padded) + beta.
+__device__ __forceinline__ void load_qka(const PrefillArgs &a, uint8_t *smem, int t0, int L, int h, int ptid) {
+    const __nv_bfloat16 *src[3] = {a.q, a.k, a.g_raw};
+#pragma unroll
+    for (int m = 0; m < 6; ++m) {
+        const int idx = ptid + kProdThreads * m;  // 0 .. 1535
+        const int tensor = idx >> 9;
+        const int row = (idx >> 4) & 31;
+        const int vec = idx & 15;
+        const bool valid = row < L;
+        const size_t tok = (size_t)(t0 + (valid ? row : 0));
+        cp_async_16(smem_addr(smem + kRawQ + tensor * 8192 + row * 256 + vec * 16),
+                    src[tensor] + (tok * a.num_heads + h) * kHeadDim + vec * 8, valid ? 16u : 0u);
+    }
+}
+
+__device__ __forceinline__ void load_vb(const PrefillArgs &a, uint8_t *smem, int t0, int L, int h, int ptid) {
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int idx = ptid + kProdThreads * m;  // 0 .. 511
+        const int row = idx >> 4, vec = idx & 15;
+        const bool valid = row < L;
+        const size_t tok = (size_t)(t0 + (valid ? row : 0));
+        cp_async_16(smem_addr(smem + kRawV + (row * kRowB + vec * 8) * 2),
+                    a.v + (tok * a.num_heads + h) * kHeadDim + vec * 8, valid ? 16u : 0u);
+    }
+    if (ptid < 32) {
+        const bool valid = ptid < L;
+        const size_t tok = (size_t)(t0 + (valid ? ptid : 0));
+        cp_async_4(smem_addr(smem + kRawBeta + ptid * 4), a.beta + tok * a.num_heads + h, valid ? 4u : 0u);
+    }
+}
+
+// ------------------------------------------------------------------ producers
+
+__device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int n, int h, int bos,
+                              int eos, int nchunks) {
+    const int ptid = threadIdx.x;  // 0 .. 255
+    const int warp = ptid >> 5, lane = ptid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    uint8_t *const pairQ = smem + kPairQ;
+    uint8_t *const pairKL = smem + kPairKL;
+    uint8_t *const pairKR = smem + kPairKR;
+    uint8_t *const kbar_s = smem + kKbar;
+    uint8_t *const qbar_s = smem + kQbar;
+    uint8_t *const wkb_s = smem + kWkB;
+    float *const wv_s = reinterpret_cast<float *>(smem + kWvS);
+    float *const ov_s = reinterpret_cast<float *>(smem + kOvS);
+    float *const am_s = reinterpret_cast<float *>(smem + kAm);
+    float *const mq_s = reinterpret_cast<float *>(smem + kMq);
+    float *const tp_s = reinterpret_cast<float *>(smem + kTp);
+    float *const t22_s = reinterpret_cast<float *>(smem + kT22);
+    float *const x_s = reinterpret_cast<float *>(smem + kXm);
+    float *const half_s = reinterpret_cast<float *>(smem + kHalf);
+    const uint8_t *const rq = smem + kRawQ;
+    const uint8_t *const rk = smem + kRawK;
+    const uint8_t *const ra = smem + kRawA;
+    const uint8_t *const rv = smem + kRawV;
+    const float *const rb = reinterpret_cast<const float *>(smem + kRawBeta);
+
+    if (nchunks > 0) {
+        const int L0 = min(kChunk, eos - bos);
+        load_qka(a, smem, bos, L0, h, ptid);
+        load_vb(a, smem, bos, L0, h, ptid);
+    }
+    cp_async_commit();
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int t0 = bos + kChunk * c;
+        const int L = min(kChunk, eos - t0);
+        const int ps = c & 1;
+        uint8_t *const stage = smem + kStage0 + ps * kStageBytes;
+        cp_async_wait<0>();
+        bar_named(kBarProd, kProdThreads);
+        if (c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status)) break;
+
+        // ---- 1. decays, anchored factors, chunk operands (thread = channel x half)
+        {
+            const int ch = ptid & 127, hf = ptid >> 7;
+            float d[16], di[16];
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) {
+                const int i = 16 * hf + ii;
+                d[ii] = di[ii] = 1.0f;
+                if (i < L) d[ii] = gate_decay_pair(bfv(ra, i * 128 + ch), a.gate_mode, a.lower_bound, di[ii]);
+            }
+            float P[16], Sx[16], fl[16], fr[16];
+            {
+                float run = 1.0f;
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) {
+                    run *= d[ii];
+                    P[ii] = run;
+                }
+                run = 1.0f;
+#pragma unroll
+                for (int ii = 15; ii >= 0; --ii) {
+                    Sx[ii] = run;
+                    run *= d[ii];
+                }
+                fl[7] = fr[7] = 1.0f;
+#pragma unroll
+                for (int ii = 8; ii < 16; ++ii) {
+                    fl[ii] = fl[ii - 1] * d[ii];
+                    fr[ii] = fr[ii - 1] * di[ii];
+                }
+#pragma unroll
+                for (int ii = 6; ii >= 0; --ii) {
+                    fl[ii] = fl[ii + 1] * di[ii + 1];
+                    fr[ii] = fr[ii + 1] * d[ii + 1];
+                }
+            }
+            half_s[hf * 128 + ch] = P[15];
+            bar_named(kBarProd, kProdThreads);
+            const float D0 = half_s[ch], D1 = half_s[128 + ch];
+            bool ok = true;
+            float krv[16];
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) {
+                const int i = 16 * hf + ii;
+                const float kk = bfv(rk, i * 128 + ch);
+                const float qq = a.scale * bfv(rq, i * 128 + ch);
+                ok &= (fl[ii] < 3.0e38f) && (fr[ii] < 3.0e38f);
+                st_bf16(pairQ, i * kRowB + ch, qq * fl[ii]);
+                st_bf16(pairKL, i * kRowB + ch, kk * fl[ii]);
+                st_bf16(pairKR, i * kRowB + ch, kk * fr[ii]);
+                float fbar, fkr;
+                if (hf) {
+                    st_bf16(pairQ, (32 + ii) * kRowB + ch, qq * P[ii]);   // 2^(G_i - G_15)
+                    st_bf16(pairKL, (32 + ii) * kRowB + ch, kk * P[ii]);
+                    fbar = D0 * P[ii];
+                    fkr = Sx[ii];
+                } else {
+                    st_bf16(pairKR, (32 + ii) * kRowB + ch, kk * Sx[ii]);  // 2^(G_15 - G_j)
+                    fbar = P[ii];
+                    fkr = Sx[ii] * D1;
+                }
+                st_bf16(kbar_s, i * kRowB + ch, kk * fbar);
+                st_bf16(qbar_s, i * kRowB + ch, qq * fbar);
+                krv[ii] = __uint_as_float(to_tf32(kk * fkr));
+            }
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                const int i0 = 16 * hf + 4 * qd;
+                *reinterpret_cast<float4 *>(stage + kStKr + core_off_tf32(ch, i0, 1024)) =
+                    make_float4(krv[4 * qd], krv[4 * qd + 1], krv[4 * qd + 2], krv[4 * qd + 3]);
+            }
+            if (!ok) report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
+            if (hf == 0) reinterpret_cast<float *>(stage + kStDec)[ch] = D0 * D1;
+        }
+        bar_named(kBarProd, kProdThreads);
+        if (c + 1 < nchunks) {
+            const int t1 = t0 + kChunk;
+            load_qka(a, smem, t1, min(kChunk, eos - t1), h, ptid);
+        }
+        cp_async_commit();
+
+        // ---- 2. Mqk (causal) and Diag(beta) A: three 16x16 blocks each (warps 0-5)
+        if (warp < 6) {
+            const int which = warp / 3;
+            const int blk = warp % 3;
+            const uint8_t *Lb = which ? pairKL : pairQ;
+            const int row0 = 16 * blk;
+            float acc[2][4] = {};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t af[4], bfr[4];
+                ldsm_x4(af, smem_addr(Lb + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
+                ldsm_x4(bfr, smem_addr(pairKR + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
+                                                  ((lane >> 3) & 1) * 8) * 2));
+                mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
+                mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
+            }
+            const int oi = (blk == 0) ? 0 : 16;
+            const int oj = (blk == 1) ? 16 : 0;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = oi + g + 8 * (e >> 1);
+                    const int j = oj + 8 * nt + 2 * t4 + (e & 1);
+                    const float val = acc[nt][e];
+                    if (which == 0) {
+                        mq_s[i * kSq + j] = (j <= i) ? val : 0.0f;
+                    } else {
+                        am_s[i * kSq + j] = (j < i) ? val * rb[i] : 0.0f;
+                    }
+                }
+            }
+        } else {
+            for (int idx = ptid - 192; idx < 256; idx += 64) {
+                const int i = idx >> 4, j = 16 + (idx & 15);
+                mq_s[i * kSq + j] = 0.0f;
+                am_s[i * kSq + j] = 0.0f;
+            }
+        }
+        bar_named(kBarProd, kProdThreads);
+
+        // ---- 3. T' = (I + Diag(beta) A)^-1 Diag(beta)
+        if (warp < 2) {
+            const int o = 16 * warp;
+            const int j = lane & 15;
+            float x[16];
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) x[ii] = (ii == j) ? 1.0f : 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+#pragma unroll
+                for (int ii = kk + 1; ii < 16; ++ii) x[ii] = fmaf(-am_s[(o + ii) * kSq + o + kk], x[kk], x[ii]);
+            }
+            if (lane < 16) {
+                const float bj = rb[o + j];
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) tp_s[(o + ii) * kSq + o + j] = x[ii] * bj;
+                if (warp == 1) {
+#pragma unroll
+                    for (int ii = 0; ii < 16; ++ii) t22_s[ii * kSmall + j] = x[ii];
+                }
+            }
+        }
+        bar_named(kBarProd, kProdThreads);
+        {
+            const int i = ptid >> 4, j = ptid & 15;
+            float s = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) s = fmaf(am_s[(16 + i) * kSq + kk], tp_s[kk * kSq + j], s);
+            x_s[i * kSmall + j] = s;
+        }
+        bar_named(kBarProd, kProdThreads);
+        {
+            const int i = ptid >> 4, j = ptid & 15;
+            float s = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) s = fmaf(t22_s[i * kSmall + kk], x_s[kk * kSmall + j], s);
+            tp_s[(16 + i) * kSq + j] = -s;
+            tp_s[i * kSq + 16 + j] = 0.0f;
+        }
+        bar_named(kBarProd, kProdThreads);
+
+        // ---- 4. Wk = T' Kbar (-> stage W rows 0-31 as -Wk, and bf16 copy), Wv = T' V (hi/lo)
+        {
+            uint32_t ah[2][2][4], al[2][2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = 16 * mt + g + 8 * (r & 1);
+                        const int col = 16 * ks + 2 * t4 + 8 * (r >> 1);
+                        const float2 v2 = *reinterpret_cast<const float2 *>(tp_s + row * kSq + col);
+                        ah[mt][ks][r] = pack_bf16(v2.x, v2.y);
+                        al[mt][ks][r] = pack_bf16(v2.x - bf16_round(v2.x), v2.y - bf16_round(v2.y));
+                    }
+                }
+            }
+            float wk[2][2][4] = {}, wvv[2][2][4] = {};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t bk[4], bv[4];
+                const int krow = 16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int ncol = 16 * warp + (lane >> 4) * 8;
+                ldsm_x4_trans(bk, smem_addr(kbar_s + (krow * kRowB + ncol) * 2));
+                ldsm_x4_trans(bv, smem_addr(rv + (krow * kRowB + ncol) * 2));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                    for (int nl = 0; nl < 2; ++nl) {
+                        mma_bf16_16816(wk[mt][nl], ah[mt][ks], bk[2 * nl], bk[2 * nl + 1]);
+                        mma_bf16_16816(wvv[mt][nl], ah[mt][ks], bv[2 * nl], bv[2 * nl + 1]);
+                        mma_bf16_16816(wvv[mt][nl], al[mt][ks], bv[2 * nl], bv[2 * nl + 1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                for (int nl = 0; nl < 2; ++nl) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int row = 16 * mt + g + 8 * hr;
+                        const int col = 16 * warp + 8 * nl + 2 * t4;
+                        const float w0 = wk[mt][nl][2 * hr], w1 = wk[mt][nl][2 * hr + 1];
+                        *reinterpret_cast<float2 *>(stage + kStW + core_off_tf32(row, col, 4096)) =
+                            make_float2(__uint_as_float(to_tf32(-w0)), __uint_as_float(to_tf32(-w1)));
+                        *reinterpret_cast<uint32_t *>(wkb_s + (row * kRowB + col) * 2) = pack_bf16(w0, w1);
+                        *reinterpret_cast<float2 *>(wv_s + row * kRowF + col) =
+                            make_float2(wvv[mt][nl][2 * hr], wvv[mt][nl][2 * hr + 1]);
+                    }
+                }
+            }
+        }
+        bar_named(kBarProd, kProdThreads);
+        if (c + 1 < nchunks) {
+            const int t1 = t0 + kChunk;
+            load_vb(a, smem, t1, min(kChunk, eos - t1), h, ptid);
+        }
+        cp_async_commit();
+
+        // ---- 5. Q' = Qbar - Mqk Wk (-> stage W rows 32-63), Ov = Mqk Wv
+        {
+            uint32_t am[2][2][4], amn[2][2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = 16 * mt + g + 8 * (r & 1);
+                        const int col = 16 * ks + 2 * t4 + 8 * (r >> 1);
+                        const float2 v2 = *reinterpret_cast<const float2 *>(mq_s + row * kSq + col);
+                        am[mt][ks][r] = pack_bf16(v2.x, v2.y);
+                        amn[mt][ks][r] = pack_bf16(-v2.x, -v2.y);
+                    }
+                }
+            }
+            float qa[2][2][4], oa[2][2][4] = {};
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                for (int nl = 0; nl < 2; ++nl) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int row = 16 * mt + g + 8 * hr;
+                        const int col = 16 * warp + 8 * nl + 2 * t4;
+                        qa[mt][nl][2 * hr] = bfv(qbar_s, row * kRowB + col);
+                        qa[mt][nl][2 * hr + 1] = bfv(qbar_s, row * kRowB + col + 1);
+                    }
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t bw[4];
+                const int krow = 16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8;
+                ldsm_x4_trans(bw, smem_addr(wkb_s + (krow * kRowB + 16 * warp + (lane >> 4) * 8) * 2));
+                uint32_t bv[2][2];
+#pragma unroll
+                for (int nl = 0; nl < 2; ++nl) {
+                    const int col = 16 * warp + 8 * nl + g;
+                    const int k0 = 16 * ks + 2 * t4;
+                    bv[nl][0] = pack_bf16(wv_s[k0 * kRowF + col], wv_s[(k0 + 1) * kRowF + col]);
+                    bv[nl][1] = pack_bf16(wv_s[(k0 + 8) * kRowF + col], wv_s[(k0 + 9) * kRowF + col]);
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                    for (int nl = 0; nl < 2; ++nl) {
+                        mma_bf16_16816(qa[mt][nl], amn[mt][ks], bw[2 * nl], bw[2 * nl + 1]);
+                        mma_bf16_16816(oa[mt][nl], am[mt][ks], bv[nl][0], bv[nl][1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                for (int nl = 0; nl < 2; ++nl) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int row = 16 * mt + g + 8 * hr;
+                        const int col = 16 * warp + 8 * nl + 2 * t4;
+                        *reinterpret_cast<float2 *>(stage + kStW + core_off_tf32(32 + row, col, 4096)) =
+                            make_float2(__uint_as_float(to_tf32(qa[mt][nl][2 * hr])),
+                                        __uint_as_float(to_tf32(qa[mt][nl][2 * hr + 1])));
+                        *reinterpret_cast<float2 *>(ov_s + row * kRowF + col) =
+                            make_float2(oa[mt][nl][2 * hr], oa[mt][nl][2 * hr + 1]);
+                    }
+                }
+            }
+        }
+        bar_named(kBarProd, kProdThreads);
+
+        // ---- 6. Wv^T / Ov^T into the chunk's D1 buffer (needs its previous use read out)
+        const int db = c & 1;
+        if (c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status)) break;
+        tc_fence_after();
+        {
+            const float *src = (warp < 4) ? wv_s : ov_s;
+            const int quad = warp & 3;
+            const int dv = 32 * quad + lane;
+            float v0[16], v1[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                v0[t] = src[t * kRowF + dv];
+                v1[t] = src[(16 + t) * kRowF + dv];
+            }
+            const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + kColD1 + 64 * db + 32 * (warp >> 2);
+            tmem_st16(taddr, v0);
+            tmem_st16(taddr + 16, v1);
+            tmem_wait_st();
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&B->prep[ps]);
+    }
+    cp_async_wait<0>();
+}
+
+// ------------------------------------------------------------------ state warps
+
+__device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int chain, int h,
+                           int bos, int eos, int nchunks) {
+    const int stid = threadIdx.x - kProdThreads;  // 0 .. 127
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3;
+    const int dv = 32 * quad + lane;
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    const bool mma_thread = (warp == kFirstStateWarp) && (lane == 0);
+    uint8_t *const ost = smem + kOst;
+    const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
+
+    // initial state -> S^T buffer 0 (lane = dv, column = dk)
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            v[e] = a.init_state ? a.init_state[sbase + (size_t)(16 * j + e) * kHeadDim + dv] : 0.0f;
+        tmem_st16(tmem + lane_base + kColS + 16 * j, v);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    bar_named(kBarState, kStateThreads);
+    tc_fence_after();
+
+    bool alive = true;
+    for (int c = 0; c < nchunks && alive; ++c) {
+        const int ps = c & 1, db = c & 1;
+        const uint32_t cur = kColS + 128 * (c & 1), nxt = kColS + 128 * ((c + 1) & 1);
+        const uint8_t *stage = smem + kStage0 + ps * kStageBytes;
+        if (!wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status)) break;
+        if (c >= 1 && !wait_or_abort(&B->g2, (c - 1) & 1, B, a.status)) break;
+        tc_fence_after();
+        if (mma_thread) {
+            const uint32_t wbase = smem_addr(stage + kStW);
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+                mma_tf32_ts(tmem + kColD1 + 64 * db, tmem + cur + 8 * s, smem_desc_kmajor(wbase + 256 * s, 128, 4096),
+                            kIdescG1, true);
+            mma_commit(&B->g1);
+        }
+        __syncwarp();
+        // decay into the other state buffer while the projection reads this one
+        {
+            const float *dec = reinterpret_cast<const float *>(stage + kStDec);
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + cur + 16 * j, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] *= dec[16 * j + e];
+                tmem_st16(tmem + lane_base + nxt + 16 * j, v);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        bar_named(kBarState, kStateThreads);
+        tc_fence_after();
+        if (mma_thread) {
+            if (wait_or_abort(&B->g1, c & 1, B, a.status)) {
+                tc_fence_after();
+                const uint32_t kbase = smem_addr(stage + kStKr);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_tf32_ts(tmem + nxt, tmem + kColD1 + 64 * db + 8 * s,
+                                smem_desc_kmajor(kbase + 256 * s, 128, 1024), kIdescG2, true);
+                mma_commit(&B->g2);
+                mma_commit(&B->g2s[ps]);
+            }
+        }
+        __syncwarp();
+        // output read-out: O^T = D1^T[:, 32:64]
+        if (!wait_or_abort(&B->g1, c & 1, B, a.status)) break;
+        tc_fence_after();
+        float o0[16], o1[16];
+        tmem_ld16(tmem + lane_base + kColD1 + 64 * db + 32, o0);
+        tmem_ld16(tmem + lane_base + kColD1 + 64 * db + 48, o1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&B->oread[db]);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            st_bf16(ost, t * kRowB + dv, o0[t]);
+            st_bf16(ost, (16 + t) * kRowB + dv, o1[t]);
+        }
+        bar_named(kBarState, kStateThreads);
+        const int t0 = bos + kChunk * c;
+        const int L = min(kChunk, eos - t0);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int idx = stid + kStateThreads * m;
+            const int row = idx >> 4, vec = idx & 15;
+            if (row < L) {
+                const uint4 v4 = *reinterpret_cast<const uint4 *>(ost + (row * kRowB + vec * 8) * 2);
+                *reinterpret_cast<uint4 *>(a.out + ((size_t)(t0 + row) * a.num_heads + h) * kHeadDim + vec * 8) = v4;
+            }
+        }
+        bar_named(kBarState, kStateThreads);
+        alive = B->abort == 0;
+    }
+
+    // final state (after the last update has completed)
+    if (B->abort == 0) {
+        if (nchunks > 0 && !wait_or_abort(&B->g2, (nchunks - 1) & 1, B, a.status)) return;
+        tc_fence_after();
+        if (a.final_state != nullptr) {
+            const uint32_t fin = kColS + 128 * (nchunks & 1);
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + fin + 16 * j, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) a.final_state[sbase + (size_t)(16 * j + e) * kHeadDim + dv] = v[e];
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    Bars *B = reinterpret_cast<Bars *>(smem + kBars);
+    const int warp = threadIdx.x >> 5;
+    const int H = a.num_heads;
+    const int chain = blockIdx.x;
+    const int n = chain / H;
+    const int h = chain - n * H;
+
+    int bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
+    if (bos < 0 || eos < bos || eos > a.total_tokens) {
+        if (threadIdx.x == 0 && h == 0) report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
+        bos = min(max(bos, 0), a.total_tokens);
+        eos = min(max(eos, bos), a.total_tokens);
+    }
+    const int nchunks = (eos - bos + kChunk - 1) / kChunk;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&B->prep[0], kProdThreads);
+        mbar_init(&B->prep[1], kProdThreads);
+        mbar_init(&B->g1, 1);
+        mbar_init(&B->g2, 1);
+        mbar_init(&B->g2s[0], 1);
+        mbar_init(&B->g2s[1], 1);
+        mbar_init(&B->oread[0], kStateThreads);
+        mbar_init(&B->oread[1], kStateThreads);
+        B->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kFirstStateWarp) {
+        tmem_alloc(&B->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = B->tmem_base;
+
+    if (warp < kProducerWarps) {
+        producer_loop(a, smem, B, tmem, n, h, bos, eos, nchunks);
+    } else {
+        state_loop(a, smem, B, tmem, chain, h, bos, eos, nchunks);
+        if (B->abort != 0 && warp == kFirstStateWarp && (threadIdx.x & 31) == 0) {
+            // drain any MMA still in flight before the tensor memory is released
+            mma_commit(&B->g1);
+            mbar_wait(&B->g1, 0);
+            mbar_wait(&B->g1, 1);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kFirstStateWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    const int64_t chains = (int64_t)a.num_seqs * a.num_heads;
+    kda_prefill_tc_kernel<<<(unsigned)chains, kThreadsTc, kSmemTc, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

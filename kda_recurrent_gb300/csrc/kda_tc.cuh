@@ -13,7 +13,7 @@
 
 namespace kda {
 
-constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr uint32_t kSpinLimit = 1u << 22;
 
 // ---------------------------------------------------------------- mbarrier
 

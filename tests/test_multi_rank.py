@@ -44,7 +44,7 @@ def _worker(rank, world, port, results):
 def test_two_rank_max_timing_and_distinct_inputs():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.spawn(_worker, args=(world, port, results), nprocs=world, join=True)
         res = dict(results)
