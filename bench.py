@@ -55,6 +55,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--seqlens", default=None,
+                   help="comma-separated sequence lengths replacing the prefill workload's (small ncu cases)")
+    p.add_argument("--heads", type=int, default=None, help="head count replacing the prefill workload's")
     return p.parse_args(argv)
 
 
@@ -160,9 +163,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workloads
 
-def prefill_workload(name, device, seed_offset=0):
+def prefill_workload(name, device, seed_offset=0, seqlens=None, heads=None):
+    import dataclasses
+
     import kda_synth as S
     cfg = S.configs()[name]
+    if seqlens or heads:
+        cfg = dataclasses.replace(cfg, name=f"{name}[seqlens={seqlens or cfg.seqlens},heads={heads or cfg.num_heads}]",
+                                  seqlens=list(seqlens or cfg.seqlens), num_heads=heads or cfg.num_heads)
     inp = S.prefill_inputs(cfg.seqlens, cfg.num_heads, seed=rank_seed(cfg.seed, seed_offset), init_std=cfg.init_std,
                            device=device)
     return cfg, inp
@@ -207,7 +215,8 @@ def run_ours(args):
     K.load(build_if_missing=True)
     peaks, peak_src = load_peaks()
 
-    pcfg, pin = prefill_workload(args.prefill, device, rank)
+    seqlens = [int(x) for x in args.seqlens.split(",")] if args.seqlens else None
+    pcfg, pin = prefill_workload(args.prefill, device, rank, seqlens, args.heads)
     dcfg, pool, din = decode_workload(args.decode_rows, args.state_dtype, device, rank)
     scale = pcfg.scale
     out = torch.empty_like(pin["q"])
@@ -283,15 +292,19 @@ def run_ours(args):
     d_gbs = d_bytes / (d_mean * 1e-3) / 1e9
     p_tflops = prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD / (p_mean * 1e-3) / 1e12
     traffic = load_traffic()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    waves = math.ceil(len(pcfg.seqlens) * pcfg.num_heads / sms)  # one CTA per chain, one CTA per SM
     prefill_roof = {"bound": "hbm", "achieved": round(p_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(p_gbs / peaks["hbm_gbs"], 5), "traffic": traffic.get("kda_prefill_kernel"),
-                    "kernel": "kda_prefill_kernel", "peak_source": peak_src,
+                    "frac": round(p_gbs / peaks["hbm_gbs"], 5),
+                    "traffic": scaled_traffic(traffic, "kda_prefill_tc_kernel", prefill_units(pcfg)),
+                    "kernel": "kda_prefill_tc_kernel", "peak_source": peak_src,
                     "algorithmic_bytes_per_launch": p_bytes,
                     "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": round(p_tflops / peaks["bf16_tflops"], 5),
                                "flop_per_launch": prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD}}
     decode_roof = {"bound": "hbm", "achieved": round(d_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                   "frac": round(d_gbs / peaks["hbm_gbs"], 5), "traffic": traffic.get("kda_decode_kernel"),
+                   "frac": round(d_gbs / peaks["hbm_gbs"], 5),
+                   "traffic": scaled_traffic(traffic, "kda_decode_kernel", args.decode_rows * dcfg.num_heads),
                    "kernel": "kda_decode_kernel", "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes}
     dominant = prefill_roof if p_mean >= d_mean else decode_roof
     line = {
@@ -309,7 +322,8 @@ def run_ours(args):
                    "l2": f"flushed between steps ({flush.numel() >> 20} MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "prefill": {"value": round(p_rate, 1), "unit": "tokens*heads/s", "ms": round(p_mean, 4),
-                    "us_per_chunk_per_chain": round(p_mean * 1e3 / math.ceil(max(pcfg.seqlens) / 32), 4)},
+                    "us_per_chunk_per_chain": round(p_mean * 1e3 / (math.ceil(max(pcfg.seqlens) / 32) * waves), 4),
+                    "waves": waves},
         "decode": {"value": round(d_rate, 1), "unit": "rows*heads/s", "ms": round(d_mean, 4), "roofline": decode_roof},
         "roofline": dominant,
         "roofline_prefill": prefill_roof,
@@ -385,15 +399,37 @@ def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist):
             "decode_unit": "rows*heads/s"}
 
 
+def source_digest(kernel_file: str) -> str:
+    import hashlib
+    with open(os.path.join(ROOT, "kda_recurrent_gb300", "csrc", kernel_file), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
 def load_traffic():
-    """Per-launch DRAM bytes of each kernel from the committed ncu summary, if current."""
+    """Per-unit DRAM bytes of each kernel from the committed ncu summary (profiles/traffic.json),
+    kept only while the kernel source still has the digest the counters were taken on."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return {k: v.get("dram_bytes_per_launch") for k, v in d.items() if v.get("current", False)}
     except (OSError, ValueError):
         return {}
+    out = {}
+    for name, rec in d.items():
+        try:
+            if source_digest(rec["source"]) == rec["source_sha256_16"]:
+                out[name] = rec
+        except (OSError, KeyError):
+            continue
+    return out
+
+
+def scaled_traffic(traffic, kernel, units):
+    """ncu DRAM bytes per launch, scaled from the captured case to this launch by units processed."""
+    rec = traffic.get(kernel)
+    if rec is None:
+        return None
+    return int(rec["dram_bytes_per_unit"] * units)
 
 
 # ------------------------------------------------------------------ oracle timing (CPU baseline)

@@ -16,14 +16,16 @@
 // reads the previous buffer.
 //
 // Warp roles (one CTA per (sequence, head) chain, 12 warps):
-//   warps 0-7  producers: raw loads (cp.async), gate and decay products, pair products and
-//              the 32 x 32 inverse (mma.sync, FP32), Wk/Wv/Q'/Ov (mma.sync), then the chunk
-//              operands into a two-deep SMEM stage ring and Wv/Ov into TMEM;
+//   warps 0-7  producers: raw loads (cp.async), gate and decay products, pair products
+//              (mma.sync), [Wk | Wv] by an FP32 forward substitution through the unit lower
+//              triangular (I + Diag(beta) A) -- the 32 x 32 inverse of the page is never formed
+//              --, Q'/Ov (mma.sync), then the chunk operands into a two-deep SMEM stage ring
+//              and Wv/Ov into TMEM;
 //   warps 8-11 state warps (one per TMEM lane quadrant): initial/final state, the decay,
 //              the output read-out and store; lane 0 of warp 8 issues the MMAs.
 // Exponent range: per 16-token half, factors are anchored at the half's 8th token, built
-// as running products of the per-token decays (no per-element exp of a prefix); the
-// off-diagonal block factors through the half boundary (both factors <= 1).
+// as running products of the per-token decays and their inverses (no per-element exp of a
+// prefix); the off-diagonal block factors through the half boundary (both factors <= 1).
 // All mbarrier waits are bounded; on expiry the kernel records KDA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
 #include "kda_internal.cuh"
@@ -45,7 +47,6 @@ constexpr int kBarState = 2;  // named barrier of the state warps
 constexpr int kRowB = 136;  // padded bf16 row stride (ldmatrix operands)
 constexpr int kRowF = 132;  // padded fp32 row stride
 constexpr int kSq = 36;     // fp32 32 x 32 tiles
-constexpr int kSmall = 20;  // fp32 16 x 16 tiles
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- shared-memory map (bytes)
@@ -65,17 +66,15 @@ constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
 constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
 constexpr int kPairEnd = kPairKR + 48 * kRowB * 2;
 constexpr int kWvS = kPair;                       // fp32 [32][132], aliases the dead pair operands
-constexpr int kOvS = kWvS + 32 * kRowF * 4;
+constexpr int kOvS = kWvS + 32 * kRowF * 4;       // fp32 [32][132]; holds Wk before it holds Ov
+constexpr int kWkS = kOvS;
 constexpr int kKbar = kPairEnd;                   // bf16 [32][136]
 constexpr int kQbar = kKbar + 32 * kRowB * 2;     // bf16 [32][136]
 constexpr int kWkB = kQbar + 32 * kRowB * 2;      // bf16 [32][136]
-constexpr int kAm = kWkB + 32 * kRowB * 2;        // fp32 [32][36]: Diag(beta) A
-constexpr int kMq = kAm + 32 * kSq * 4;           // fp32 [32][36]: Mqk
-constexpr int kTp = kMq + 32 * kSq * 4;           // fp32 [32][36]: T'
-constexpr int kT22 = kTp + 32 * kSq * 4;          // fp32 [16][20]
-constexpr int kXm = kT22 + 16 * kSmall * 4;       // fp32 [16][20]
-constexpr int kHalf = kXm + 16 * kSmall * 4;      // fp32 [2][128]
-constexpr int kOst = kHalf + 2 * 128 * 4;         // bf16 [32][136]: output staging
+constexpr int kNt = kWkB + 32 * kRowB * 2;        // fp32 [32][36]: (Diag(beta) A)^T
+constexpr int kMq = kNt + 32 * kSq * 4;           // fp32 [32][36]: Mqk
+constexpr int kQuart = kMq + 32 * kSq * 4;        // fp32 [4][128]: per-quarter decay products
+constexpr int kOst = kQuart + 4 * 128 * 4;        // bf16 [32][136]: output staging
 constexpr int kBars = kOst + 32 * kRowB * 2;
 constexpr int kSmemTc = kBars + 128;
 static_assert(kOvS + 32 * kRowF * 4 <= kPairEnd, "Wv/Ov staging fits in the pair region");
@@ -127,22 +126,41 @@ __device__ __forceinline__ int core_off_tf32(int row, int col, int sbo) {
     return (row >> 3) * sbo + (col >> 2) * 128 + (row & 7) * 16 + (col & 3) * 4;
 }
 
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Per-token decay d = exp(g) of one channel and its inverse 1/d, from the raw gate a.
 __device__ __forceinline__ float gate_decay_pair(float av, int mode, float lower_bound, float &dinv) {
-    // returns d = exp(g) and sets dinv = exp(-g)
     if (mode == KDA_GATE_LOWER_BOUND) {
-        const float s = __fdividef(1.0f, 1.0f + exp2f(-av * kLog2e));
-        const float g2 = lower_bound * s * kLog2e;
-        dinv = exp2f(-g2);
-        return exp2f(g2);
+        const float g2 = lower_bound * kLog2e * rcp(1.0f + ex2(-av * kLog2e));  // lb sigmoid(a) log2 e
+        dinv = ex2(-g2);
+        return ex2(g2);
     }
     if (mode == KDA_GATE_SOFTPLUS) {
         // exp(-softplus(a)) = 1 / (1 + e^a)
-        const float e = exp2f(av * kLog2e);
-        dinv = 1.0f + e;
-        return __fdividef(1.0f, dinv);
+        dinv = 1.0f + ex2(av * kLog2e);
+        return rcp(dinv);
     }
-    dinv = exp2f(-av * kLog2e);
-    return exp2f(av * kLog2e);
+    dinv = ex2(-av * kLog2e);
+    return ex2(av * kLog2e);
+}
+
+__device__ __forceinline__ void unpack_bf16x2(uint32_t w, float &lo, float &hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+}
+
+__device__ __forceinline__ void st_pair(uint8_t *base, int elem, float lo, float hi) {
+    *reinterpret_cast<uint32_t *>(base + 2 * elem) = pack_bf16(lo, hi);
 }
 
 // Producer-side raw loads of one chunk: q, k, a rows (unpadded) or v rows (padded) + beta.
@@ -193,12 +211,10 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     uint8_t *const wkb_s = smem + kWkB;
     float *const wv_s = reinterpret_cast<float *>(smem + kWvS);
     float *const ov_s = reinterpret_cast<float *>(smem + kOvS);
-    float *const am_s = reinterpret_cast<float *>(smem + kAm);
+    float *const wk_s = reinterpret_cast<float *>(smem + kWkS);
+    float *const nt_s = reinterpret_cast<float *>(smem + kNt);
     float *const mq_s = reinterpret_cast<float *>(smem + kMq);
-    float *const tp_s = reinterpret_cast<float *>(smem + kTp);
-    float *const t22_s = reinterpret_cast<float *>(smem + kT22);
-    float *const x_s = reinterpret_cast<float *>(smem + kXm);
-    float *const half_s = reinterpret_cast<float *>(smem + kHalf);
+    float *const quart_s = reinterpret_cast<float *>(smem + kQuart);
     const uint8_t *const rq = smem + kRawQ;
     const uint8_t *const rk = smem + kRawK;
     const uint8_t *const ra = smem + kRawA;
@@ -221,79 +237,127 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         bar_named(kBarProd, kProdThreads);
         if (c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status)) break;
 
-        // ---- 1. decays, anchored factors, chunk operands (thread = channel x half)
+        // ---- 1. decays, anchored factors, chunk operands. Thread = (channel pair, 8-token
+        //      quarter). With d the per-token decay, every factor is a running product of d or
+        //      1/d inside a quarter times whole-quarter products: 2^G_i (prefix), 2^(G_L - G_i)
+        //      (suffix), the half-chunk anchors at tokens 7 and 23 and the half boundary 15.
         {
-            const int ch = ptid & 127, hf = ptid >> 7;
-            float d[16], di[16];
+            const int cp = ptid & 63, qt = ptid >> 6;
+            const int ch = 2 * cp;
+            float d0[8], d1[8], e0[8], e1[8];
 #pragma unroll
-            for (int ii = 0; ii < 16; ++ii) {
-                const int i = 16 * hf + ii;
-                d[ii] = di[ii] = 1.0f;
-                if (i < L) d[ii] = gate_decay_pair(bfv(ra, i * 128 + ch), a.gate_mode, a.lower_bound, di[ii]);
+            for (int ii = 0; ii < 8; ++ii) {
+                const int i = 8 * qt + ii;
+                d0[ii] = d1[ii] = e0[ii] = e1[ii] = 1.0f;
+                if (i < L) {
+                    float a0, a1;
+                    unpack_bf16x2(*reinterpret_cast<const uint32_t *>(ra + 2 * (i * 128 + ch)), a0, a1);
+                    d0[ii] = gate_decay_pair(a0, a.gate_mode, a.lower_bound, e0[ii]);
+                    d1[ii] = gate_decay_pair(a1, a.gate_mode, a.lower_bound, e1[ii]);
+                }
             }
-            float P[16], Sx[16], fl[16], fr[16];
+            // P: inclusive prefix of d; S: exclusive suffix of d; F: the anchored factor made
+            // of 1/d (exclusive suffix up to the anchor in quarters 0 and 2, inclusive prefix
+            // from the anchor on in quarters 1 and 3).
+            const bool before_anchor = (qt & 1) == 0;
+            float P0[8], P1[8], S0[8], S1[8], F0[8], F1[8];
             {
-                float run = 1.0f;
+                float r0 = 1.0f, r1 = 1.0f;
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) {
-                    run *= d[ii];
-                    P[ii] = run;
+                for (int ii = 0; ii < 8; ++ii) {
+                    r0 *= d0[ii];
+                    r1 *= d1[ii];
+                    P0[ii] = r0;
+                    P1[ii] = r1;
                 }
-                run = 1.0f;
+                r0 = r1 = 1.0f;
 #pragma unroll
-                for (int ii = 15; ii >= 0; --ii) {
-                    Sx[ii] = run;
-                    run *= d[ii];
+                for (int ii = 7; ii >= 0; --ii) {
+                    S0[ii] = r0;
+                    S1[ii] = r1;
+                    r0 *= d0[ii];
+                    r1 *= d1[ii];
                 }
-                fl[7] = fr[7] = 1.0f;
+                r0 = r1 = 1.0f;
+                if (before_anchor) {
 #pragma unroll
-                for (int ii = 8; ii < 16; ++ii) {
-                    fl[ii] = fl[ii - 1] * d[ii];
-                    fr[ii] = fr[ii - 1] * di[ii];
-                }
-#pragma unroll
-                for (int ii = 6; ii >= 0; --ii) {
-                    fl[ii] = fl[ii + 1] * di[ii + 1];
-                    fr[ii] = fr[ii + 1] * d[ii + 1];
-                }
-            }
-            half_s[hf * 128 + ch] = P[15];
-            bar_named(kBarProd, kProdThreads);
-            const float D0 = half_s[ch], D1 = half_s[128 + ch];
-            bool ok = true;
-            float krv[16];
-#pragma unroll
-            for (int ii = 0; ii < 16; ++ii) {
-                const int i = 16 * hf + ii;
-                const float kk = bfv(rk, i * 128 + ch);
-                const float qq = a.scale * bfv(rq, i * 128 + ch);
-                ok &= (fl[ii] < 3.0e38f) && (fr[ii] < 3.0e38f);
-                st_bf16(pairQ, i * kRowB + ch, qq * fl[ii]);
-                st_bf16(pairKL, i * kRowB + ch, kk * fl[ii]);
-                st_bf16(pairKR, i * kRowB + ch, kk * fr[ii]);
-                float fbar, fkr;
-                if (hf) {
-                    st_bf16(pairQ, (32 + ii) * kRowB + ch, qq * P[ii]);   // 2^(G_i - G_15)
-                    st_bf16(pairKL, (32 + ii) * kRowB + ch, kk * P[ii]);
-                    fbar = D0 * P[ii];
-                    fkr = Sx[ii];
+                    for (int ii = 7; ii >= 0; --ii) {
+                        F0[ii] = r0;
+                        F1[ii] = r1;
+                        r0 *= e0[ii];
+                        r1 *= e1[ii];
+                    }
                 } else {
-                    st_bf16(pairKR, (32 + ii) * kRowB + ch, kk * Sx[ii]);  // 2^(G_15 - G_j)
-                    fbar = P[ii];
-                    fkr = Sx[ii] * D1;
+#pragma unroll
+                    for (int ii = 0; ii < 8; ++ii) {
+                        r0 *= e0[ii];
+                        r1 *= e1[ii];
+                        F0[ii] = r0;
+                        F1[ii] = r1;
+                    }
                 }
-                st_bf16(kbar_s, i * kRowB + ch, kk * fbar);
-                st_bf16(qbar_s, i * kRowB + ch, qq * fbar);
-                krv[ii] = __uint_as_float(to_tf32(kk * fkr));
+            }
+            *reinterpret_cast<float2 *>(quart_s + qt * 128 + ch) = make_float2(P0[7], P1[7]);
+            bar_named(kBarProd, kProdThreads);
+            float2 T[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) T[q4] = *reinterpret_cast<const float2 *>(quart_s + q4 * 128 + ch);
+            float pre0 = 1.0f, pre1 = 1.0f, post0 = 1.0f, post1 = 1.0f;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                if (q4 < qt) {
+                    pre0 *= T[q4].x;
+                    pre1 *= T[q4].y;
+                } else if (q4 > qt) {
+                    post0 *= T[q4].x;
+                    post1 *= T[q4].y;
+                }
+            }
+            // off-diagonal factors 2^(G_i - G_15) (i >= 16) and 2^(G_15 - G_j) (j < 16)
+            const float od0 = (qt == 0) ? T[1].x : ((qt == 3) ? T[2].x : 1.0f);
+            const float od1 = (qt == 0) ? T[1].y : ((qt == 3) ? T[2].y : 1.0f);
+            bool ok = true;
+            float kr0[8], kr1[8];
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                const int i = 8 * qt + ii;
+                float k0, k1, q0, q1;
+                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rk + 2 * (i * 128 + ch)), k0, k1);
+                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rq + 2 * (i * 128 + ch)), q0, q1);
+                q0 *= a.scale;
+                q1 *= a.scale;
+                const float fl0 = before_anchor ? F0[ii] : P0[ii], fl1 = before_anchor ? F1[ii] : P1[ii];
+                const float fr0 = before_anchor ? S0[ii] : F0[ii], fr1 = before_anchor ? S1[ii] : F1[ii];
+                ok &= (fl0 < 3.0e38f) && (fl1 < 3.0e38f) && (fr0 < 3.0e38f) && (fr1 < 3.0e38f);
+                st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
+                st_pair(pairKL, i * kRowB + ch, k0 * fl0, k1 * fl1);
+                st_pair(pairKR, i * kRowB + ch, k0 * fr0, k1 * fr1);
+                if (qt >= 2) {
+                    const float fo0 = od0 * P0[ii], fo1 = od1 * P1[ii];
+                    st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
+                    st_pair(pairKL, (16 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                } else {
+                    const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
+                    st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                }
+                const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
+                st_pair(kbar_s, i * kRowB + ch, k0 * fb0, k1 * fb1);
+                st_pair(qbar_s, i * kRowB + ch, q0 * fb0, q1 * fb1);
+                kr0[ii] = __uint_as_float(to_tf32(k0 * (S0[ii] * post0)));  // 2^(G_L - G_i)
+                kr1[ii] = __uint_as_float(to_tf32(k1 * (S1[ii] * post1)));
             }
 #pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                const int i0 = 16 * hf + 4 * qd;
+            for (int h4 = 0; h4 < 2; ++h4) {
+                const int i0 = 8 * qt + 4 * h4;
                 *reinterpret_cast<float4 *>(stage + kStKr + core_off_tf32(ch, i0, 1024)) =
-                    make_float4(krv[4 * qd], krv[4 * qd + 1], krv[4 * qd + 2], krv[4 * qd + 3]);
+                    make_float4(kr0[4 * h4], kr0[4 * h4 + 1], kr0[4 * h4 + 2], kr0[4 * h4 + 3]);
+                *reinterpret_cast<float4 *>(stage + kStKr + core_off_tf32(ch + 1, i0, 1024)) =
+                    make_float4(kr1[4 * h4], kr1[4 * h4 + 1], kr1[4 * h4 + 2], kr1[4 * h4 + 3]);
             }
             if (!ok) report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
-            if (hf == 0) reinterpret_cast<float *>(stage + kStDec)[ch] = D0 * D1;
+            if (qt == 0)
+                *reinterpret_cast<float2 *>(stage + kStDec + 4 * ch) =
+                    make_float2(T[0].x * T[1].x * T[2].x * T[3].x, T[0].y * T[1].y * T[2].y * T[3].y);
         }
         bar_named(kBarProd, kProdThreads);
         if (c + 1 < nchunks) {
@@ -302,7 +366,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         }
         cp_async_commit();
 
-        // ---- 2. Mqk (causal) and Diag(beta) A: three 16x16 blocks each (warps 0-5)
+        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5)
         if (warp < 6) {
             const int which = warp / 3;
             const int blk = warp % 3;
@@ -330,7 +394,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     if (which == 0) {
                         mq_s[i * kSq + j] = (j <= i) ? val : 0.0f;
                     } else {
-                        am_s[i * kSq + j] = (j < i) ? val * rb[i] : 0.0f;
+                        nt_s[j * kSq + i] = (j < i) ? val * rb[i] : 0.0f;
                     }
                 }
             }
@@ -338,104 +402,34 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             for (int idx = ptid - 192; idx < 256; idx += 64) {
                 const int i = idx >> 4, j = 16 + (idx & 15);
                 mq_s[i * kSq + j] = 0.0f;
-                am_s[i * kSq + j] = 0.0f;
+                nt_s[j * kSq + i] = 0.0f;
             }
         }
         bar_named(kBarProd, kProdThreads);
 
-        // ---- 3. T' = (I + Diag(beta) A)^-1 Diag(beta)
-        if (warp < 2) {
-            const int o = 16 * warp;
-            const int j = lane & 15;
-            float x[16];
-#pragma unroll
-            for (int ii = 0; ii < 16; ++ii) x[ii] = (ii == j) ? 1.0f : 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-#pragma unroll
-                for (int ii = kk + 1; ii < 16; ++ii) x[ii] = fmaf(-am_s[(o + ii) * kSq + o + kk], x[kk], x[ii]);
-            }
-            if (lane < 16) {
-                const float bj = rb[o + j];
-#pragma unroll
-                for (int ii = 0; ii < 16; ++ii) tp_s[(o + ii) * kSq + o + j] = x[ii] * bj;
-                if (warp == 1) {
-#pragma unroll
-                    for (int ii = 0; ii < 16; ++ii) t22_s[ii * kSmall + j] = x[ii];
-                }
-            }
-        }
-        bar_named(kBarProd, kProdThreads);
+        // ---- 3. (I + Diag(beta) A) [Wk | Wv] = Diag(beta) [Kbar | V] by forward substitution in
+        //      FP32, one column per thread (warps 0-3: Kbar columns, warps 4-7: V columns).
         {
-            const int i = ptid >> 4, j = ptid & 15;
-            float s = 0.0f;
+            const int cc = ptid & 127;
+            const uint8_t *X = (ptid < 128) ? kbar_s : rv;
+            float acc[32];
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) s = fmaf(am_s[(16 + i) * kSq + kk], tp_s[kk * kSq + j], s);
-            x_s[i * kSmall + j] = s;
-        }
-        bar_named(kBarProd, kProdThreads);
-        {
-            const int i = ptid >> 4, j = ptid & 15;
-            float s = 0.0f;
+            for (int i = 0; i < 32; ++i) acc[i] = rb[i] * bfv(X, i * kRowB + cc);
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) s = fmaf(t22_s[i * kSmall + kk], x_s[kk * kSmall + j], s);
-            tp_s[(16 + i) * kSq + j] = -s;
-            tp_s[i * kSq + 16 + j] = 0.0f;
-        }
-        bar_named(kBarProd, kProdThreads);
-
-        // ---- 4. Wk = T' Kbar (-> stage W rows 0-31 as -Wk, and bf16 copy), Wv = T' V (hi/lo)
-        {
-            uint32_t ah[2][2][4], al[2][2][4];
+            for (int j = 0; j < 31; ++j) {
+                const float wj = acc[j];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = 16 * mt + g + 8 * (r & 1);
-                        const int col = 16 * ks + 2 * t4 + 8 * (r >> 1);
-                        const float2 v2 = *reinterpret_cast<const float2 *>(tp_s + row * kSq + col);
-                        ah[mt][ks][r] = pack_bf16(v2.x, v2.y);
-                        al[mt][ks][r] = pack_bf16(v2.x - bf16_round(v2.x), v2.y - bf16_round(v2.y));
-                    }
+                for (int m = (j + 1) >> 2; m < 8; ++m) {
+                    const float4 n4 = *reinterpret_cast<const float4 *>(nt_s + j * kSq + 4 * m);
+                    if (4 * m + 0 > j) acc[4 * m + 0] = fmaf(-n4.x, wj, acc[4 * m + 0]);
+                    if (4 * m + 1 > j) acc[4 * m + 1] = fmaf(-n4.y, wj, acc[4 * m + 1]);
+                    if (4 * m + 2 > j) acc[4 * m + 2] = fmaf(-n4.z, wj, acc[4 * m + 2]);
+                    if (4 * m + 3 > j) acc[4 * m + 3] = fmaf(-n4.w, wj, acc[4 * m + 3]);
                 }
             }
-            float wk[2][2][4] = {}, wvv[2][2][4] = {};
+            float *dst = (ptid < 128) ? wk_s : wv_s;
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                uint32_t bk[4], bv[4];
-                const int krow = 16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int ncol = 16 * warp + (lane >> 4) * 8;
-                ldsm_x4_trans(bk, smem_addr(kbar_s + (krow * kRowB + ncol) * 2));
-                ldsm_x4_trans(bv, smem_addr(rv + (krow * kRowB + ncol) * 2));
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                    for (int nl = 0; nl < 2; ++nl) {
-                        mma_bf16_16816(wk[mt][nl], ah[mt][ks], bk[2 * nl], bk[2 * nl + 1]);
-                        mma_bf16_16816(wvv[mt][nl], ah[mt][ks], bv[2 * nl], bv[2 * nl + 1]);
-                        mma_bf16_16816(wvv[mt][nl], al[mt][ks], bv[2 * nl], bv[2 * nl + 1]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                for (int nl = 0; nl < 2; ++nl) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int row = 16 * mt + g + 8 * hr;
-                        const int col = 16 * warp + 8 * nl + 2 * t4;
-                        const float w0 = wk[mt][nl][2 * hr], w1 = wk[mt][nl][2 * hr + 1];
-                        *reinterpret_cast<float2 *>(stage + kStW + core_off_tf32(row, col, 4096)) =
-                            make_float2(__uint_as_float(to_tf32(-w0)), __uint_as_float(to_tf32(-w1)));
-                        *reinterpret_cast<uint32_t *>(wkb_s + (row * kRowB + col) * 2) = pack_bf16(w0, w1);
-                        *reinterpret_cast<float2 *>(wv_s + row * kRowF + col) =
-                            make_float2(wvv[mt][nl][2 * hr], wvv[mt][nl][2 * hr + 1]);
-                    }
-                }
-            }
+            for (int i = 0; i < 32; ++i) dst[i * kRowF + cc] = acc[i];
         }
         bar_named(kBarProd, kProdThreads);
         if (c + 1 < nchunks) {
@@ -443,6 +437,22 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             load_vb(a, smem, t1, min(kChunk, eos - t1), h, ptid);
         }
         cp_async_commit();
+
+        // ---- 4. -Wk into the stage's W rows 0-31 (tf32 core matrices; lanes walk the 8 rows of
+        //      a core matrix so the stores are contiguous) and a bf16 copy of Wk for step 5.
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int idx = ptid + kProdThreads * m;  // 0 .. 1023
+            const int row = ((idx >> 8) << 3) + (idx & 7);
+            const int grp = (idx >> 3) & 31;
+            const float4 w = *reinterpret_cast<const float4 *>(wk_s + row * kRowF + 4 * grp);
+            *reinterpret_cast<float4 *>(stage + kStW + core_off_tf32(row, 4 * grp, 4096)) =
+                make_float4(__uint_as_float(to_tf32(-w.x)), __uint_as_float(to_tf32(-w.y)),
+                            __uint_as_float(to_tf32(-w.z)), __uint_as_float(to_tf32(-w.w)));
+            *reinterpret_cast<uint2 *>(wkb_s + (row * kRowB + 4 * grp) * 2) =
+                make_uint2(pack_bf16(w.x, w.y), pack_bf16(w.z, w.w));
+        }
+        bar_named(kBarProd, kProdThreads);
 
         // ---- 5. Q' = Qbar - Mqk Wk (-> stage W rows 32-63), Ov = Mqk Wv
         {

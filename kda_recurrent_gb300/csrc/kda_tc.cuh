@@ -5,15 +5,22 @@
 //    quadrant 32 * (warp % 4) with the 32x32b access shapes.
 //  * MMAs are issued by one thread; completion is observed through tcgen05.commit
 //    arriving on an mbarrier.
-//  * Every mbarrier wait is bounded: after `kSpinLimit` polls it gives up and reports
-//    false, so a lost arrival can never hang the GPU.
+//  * Every mbarrier wait is bounded: after kWaitLimitNs of wall-clock time it gives up
+//    and reports false, so a lost arrival can never hang the GPU.
 #pragma once
 
 #include <stdint.h>
 
 namespace kda {
 
-constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait that lasts 2 s is treated as lost
+constexpr uint32_t kSuspendHintNs = 1000000u;      // hardware suspend hint per try_wait
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -32,21 +39,28 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
         : "memory");
 }
 
-// Polls phase `parity` of `bar`; false if the spin limit ran out.
+// Waits for phase `parity` of `bar` with the thread suspended in hardware between
+// polls; false if it has not completed after kWaitLimitNs of wall-clock time.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     const uint32_t addr = smem_addr(bar);
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint64_t start = 0;
+    for (;;) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(addr), "r"(parity)
+            : "r"(addr), "r"(parity), "r"(kSuspendHintNs)
             : "memory");
         if (done) return true;
+        const uint64_t now = global_ns();
+        if (start == 0) {
+            start = now;
+        } else if (now - start > kWaitLimitNs) {
+            return false;
+        }
     }
-    return false;
 }
 
 // ---------------------------------------------------------------- TMEM allocation
