@@ -58,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--seqlens", default=None,
                    help="comma-separated sequence lengths replacing the prefill workload's (small ncu cases)")
     p.add_argument("--heads", type=int, default=None, help="head count replacing the prefill workload's")
+    p.add_argument("--pool-slots", type=int, default=None, help="decode pool size replacing 16384 (small ncu cases)")
+    p.add_argument("--no-windows", action="store_true",
+                   help="run kda_prefill (sequential chunk loop) instead of kda_prefill_ex with a workspace")
     return p.parse_args(argv)
 
 
@@ -176,9 +179,13 @@ def prefill_workload(name, device, seed_offset=0, seqlens=None, heads=None):
     return cfg, inp
 
 
-def decode_workload(rows, state_dtype, device, seed_offset=0):
+def decode_workload(rows, state_dtype, device, seed_offset=0, pool_slots=None):
+    import dataclasses
+
     import kda_synth as S
     cfg = S.configs()["decode_h8_pool16384"]
+    if pool_slots:
+        cfg = dataclasses.replace(cfg, num_slots=pool_slots)
     seed = rank_seed(cfg.seed, seed_offset)
     pool = S.state_pool(cfg.num_slots, cfg.num_heads, state_dtype, std=cfg.pool_std, seed=seed, device=device)
     inp = S.decode_inputs(rows, cfg.num_heads, seed=seed, device=device)
@@ -217,7 +224,7 @@ def run_ours(args):
 
     seqlens = [int(x) for x in args.seqlens.split(",")] if args.seqlens else None
     pcfg, pin = prefill_workload(args.prefill, device, rank, seqlens, args.heads)
-    dcfg, pool, din = decode_workload(args.decode_rows, args.state_dtype, device, rank)
+    dcfg, pool, din = decode_workload(args.decode_rows, args.state_dtype, device, rank, args.pool_slots)
     scale = pcfg.scale
     out = torch.empty_like(pin["q"])
     fin = torch.empty(len(pcfg.seqlens), pcfg.num_heads, 128, 128, dtype=torch.float32, device=device)
@@ -225,10 +232,13 @@ def run_ours(args):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(max(2 * l2, 512 << 20), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
+    ws = None if args.no_windows else K.prefill_workspace(len(pcfg.seqlens), pcfg.total_tokens, pcfg.num_heads,
+                                                          device)
+    prefill_launches = 3 if ws is not None else 1  # window pass + carry + output pass, or the chunk loop
 
     def prefill_call():
-        K.kda_prefill(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta"], pin["cu_seqlens"], pin["init_state"],
-                      out, fin, scale, pcfg.lower_bound, pcfg.gate_mode, stream)
+        K.kda_prefill_ex(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta"], pin["cu_seqlens"],
+                         pin["init_state"], out, fin, scale, pcfg.lower_bound, pcfg.gate_mode, ws, stream)
 
     def decode_call():
         K.kda_decode(din["q"], din["k"], din["v"], din["g_raw"], din["beta"], din["slot_idx"], pool, dout, dcfg.scale,
@@ -272,7 +282,7 @@ def run_ours(args):
     if st != K.KDA_OK:
         raise RuntimeError(f"device status {st} ({detail}) after the timed region")
 
-    e2e = None if args.no_e2e else measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist)
+    e2e = None if args.no_e2e else measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws)
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(pcfg, pin, dcfg, din, pool)
@@ -296,8 +306,10 @@ def run_ours(args):
     waves = math.ceil(len(pcfg.seqlens) * pcfg.num_heads / sms)  # one CTA per chain, one CTA per SM
     prefill_roof = {"bound": "hbm", "achieved": round(p_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(p_gbs / peaks["hbm_gbs"], 5),
-                    "traffic": scaled_traffic(traffic, "kda_prefill_tc_kernel", prefill_units(pcfg)),
-                    "kernel": "kda_prefill_tc_kernel", "peak_source": peak_src,
+                    "traffic": (scaled_traffic(traffic, "kda_prefill_tc_kernel", prefill_units(pcfg))
+                                if ws is None else None),
+                    "kernel": ("kda_prefill_tc_kernel" if ws is None else
+                               "kda_prefill_ex window schedule (window pass + carry + output pass)"), "peak_source": peak_src,
                     "algorithmic_bytes_per_launch": p_bytes,
                     "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": round(p_tflops / peaks["bf16_tflops"], 5),
@@ -312,13 +324,15 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(p_mean + d_mean, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool16384",
+        "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool{dcfg.num_slots}",
                    "prefill": {"seqlens": pcfg.seqlens if len(pcfg.seqlens) <= 16 else f"{len(pcfg.seqlens)} seqs",
                                "heads": pcfg.num_heads, "gate": pcfg.gate_mode, "lower_bound": pcfg.lower_bound,
                                "init_state": pcfg.init_std is not None},
                    "decode": {"rows": args.decode_rows, "heads": dcfg.num_heads, "pool_slots": dcfg.num_slots,
                               "state_dtype": args.state_dtype},
                    "precision": "bf16 operands, tf32 state update, fp32 state and accumulation",
+                   "prefill_schedule": ("sequential chunk loop" if ws is None else
+                                        f"windows ({ws.numel() >> 20} MiB workspace)"),
                    "l2": f"flushed between steps ({flush.numel() >> 20} MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "prefill": {"value": round(p_rate, 1), "unit": "tokens*heads/s", "ms": round(p_mean, 4),
@@ -327,7 +341,7 @@ def run_ours(args):
         "decode": {"value": round(d_rate, 1), "unit": "rows*heads/s", "ms": round(d_mean, 4), "roofline": decode_roof},
         "roofline": dominant,
         "roofline_prefill": prefill_roof,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (prefill_launches + 1) * args.steps,
         "wall_s_timed_region": round(wall, 4),
     }
     if sampler:
@@ -341,7 +355,7 @@ def run_ours(args):
     return line
 
 
-def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist):
+def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws):
     """Same metric through the C ABI from pinned host buffers: H2D of the step's inputs,
     the two calls, D2H of the outputs (prefill out + final state, decode out)."""
     import torch
@@ -364,8 +378,8 @@ def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist):
         for k2, v in host_p.items():
             if v is not None:
                 dev_p[k2].copy_(v, non_blocking=True)
-        K.kda_prefill(dev_p["q"], dev_p["k"], dev_p["v"], dev_p["g_raw"], dev_p["beta"], dev_p["cu_seqlens"],
-                      dev_p["init_state"], out, fin, pcfg.scale, pcfg.lower_bound, pcfg.gate_mode, stream)
+        K.kda_prefill_ex(dev_p["q"], dev_p["k"], dev_p["v"], dev_p["g_raw"], dev_p["beta"], dev_p["cu_seqlens"],
+                         dev_p["init_state"], out, fin, pcfg.scale, pcfg.lower_bound, pcfg.gate_mode, ws, stream)
         h_out.copy_(out, non_blocking=True)
         h_fin.copy_(fin, non_blocking=True)
 
@@ -505,7 +519,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(wall * 1e3 / max(1, args.steps), 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool16384",
+            "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool{dcfg.num_slots}",
                        "note": "FP64 CPU oracle on bounded samples of the workload"},
             "decode": {"value": round(statistics.median(d_rates), 2), "unit": "rows*heads/s"},
             "cpu_baseline": {"value": round(p_rate, 2), "unit": "tokens*heads/s", "cores": r["prefill"][1],

@@ -113,6 +113,37 @@ KDA_API int kda_prefill(const void *q, const void *k, const void *v, const void 
                 kda_stream_t stream);
 
 /*
+ * kda_prefill_workspace_size -- bytes of device workspace kda_prefill_ex uses for a call
+ * of this shape; 0 means it would not use any (the chains already fill the GPU).
+ *   sm_count  multiprocessors of the device the call will run on; 0 = ask the current
+ *             device (a CUDA call). With sm_count > 0 this is pure host arithmetic.
+ * Returns the byte count, or a negative kda_status (KDA_ERR_INVALID_ARG for bad sizes,
+ * KDA_ERR_CUDA if the device query fails).
+ */
+KDA_API int64_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                           int32_t sm_count);
+
+/*
+ * kda_prefill_ex -- kda_prefill with a caller-owned device workspace (16-byte aligned).
+ * When the (sequence, head) chains are too few to fill the GPU, each chain's chunks are
+ * cut into windows that run in parallel, in the spirit of the windowed "affine
+ * composite" of FlashInfer PR #5573 ("1. Composite schedule"): a window pass computes,
+ * from a zero start, each window's end state E and linear map M (S_end = M S_start + E);
+ * an FP32 carry pass walks the windows of each chain; the output pass then reruns every
+ * window from its true start state. Results match kda_prefill up to rounding.
+ *   workspace        NULL: the sequential schedule (same as kda_prefill);
+ *                    otherwise at least kda_prefill_workspace_size(..., 0) bytes on the
+ *                    current device, or KDA_ERR_INVALID_ARG. Its contents on entry do not
+ *                    matter; calls sharing one workspace must not overlap on the GPU.
+ * All other arguments as kda_prefill.
+ */
+KDA_API int kda_prefill_ex(const void *q, const void *k, const void *v, const void *g_raw,
+                           const float *beta, const int32_t *cu_seqlens, const float *init_state,
+                           void *out, float *final_state, int32_t num_seqs, int32_t total_tokens,
+                           int32_t num_heads, float scale, float lower_bound, int32_t gate_mode,
+                           void *workspace, int64_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_decode -- one token per row (T = 1) against a slot-indexed state pool.
  *   q, k, g_raw  BF16 [rows, num_heads, 128]
  *   v            BF16 [rows, num_heads, 128]

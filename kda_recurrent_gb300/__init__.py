@@ -10,6 +10,7 @@ Low-level calls mirror the C names and take caller-owned torch tensors:
                 lower_bound, gate_mode, stream=None)
     kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound,
                gate_mode, stream=None)
+    kda_prefill_ex(..., workspace=None, stream=None), kda_prefill_workspace_size(N, T, H, sm_count=0)
     kda_status_string(status), kda_device_status(stream=None)
 Convenience wrappers ``prefill`` / ``decode`` allocate the outputs.
 """
@@ -34,7 +35,8 @@ STATE_DTYPES = {"f32": 0, "bf16": 1}
 HEAD_DIM = 128
 CHUNK = 32
 
-EXPORTED_SYMBOLS = ("kda_prefill", "kda_decode", "kda_status_string", "kda_device_status", "kda_abi_version")
+EXPORTED_SYMBOLS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_workspace_size", "kda_decode", "kda_status_string",
+                    "kda_device_status", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +66,11 @@ def load(build_if_missing: bool = False):
             vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
             lib.kda_prefill.restype = ctypes.c_int
             lib.kda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
+            lib.kda_prefill_ex.restype = ctypes.c_int
+            lib.kda_prefill_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp, i64,
+                                           vp]
+            lib.kda_prefill_workspace_size.restype = ctypes.c_int64
+            lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
             lib.kda_decode.restype = ctypes.c_int
             lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -129,6 +136,49 @@ def kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, 
         raise KdaError(st, "kda_prefill")
 
 
+def kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, sm_count=0) -> int:
+    """Workspace bytes kda_prefill_ex uses for this shape (0: none); sm_count 0 asks the current device."""
+    n = load().kda_prefill_workspace_size(int(num_seqs), int(total_tokens), int(num_heads), int(sm_count))
+    if n < 0:
+        raise KdaError(int(n), "kda_prefill_workspace_size")
+    return int(n)
+
+
+def kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, scale, lower_bound=0.0,
+                   gate_mode="lower_bound", workspace=None, stream=None):
+    """kda_prefill with a caller-owned device workspace (a uint8 tensor, or None)."""
+    import torch
+    T, H, d = q.shape
+    N = cu_seqlens.shape[0] - 1
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("out", out)):
+        _check(t, name, torch.bfloat16, (T, H, d), dev)
+    _check(beta, "beta", torch.float32, (T, H), dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    for name, t in (("init_state", init_state), ("final_state", final_state)):
+        if t is not None:
+            _check(t, name, torch.float32, (N, H, d, d), dev)
+    nbytes = 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace: must be a contiguous tensor on the inputs' device")
+        nbytes = workspace.numel() * workspace.element_size()
+    st = load().kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
+                               _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
+                               float(lower_bound), _mode(gate_mode), _ptr(workspace), nbytes,
+                               _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_ex")
+
+
+def prefill_workspace(num_seqs, total_tokens, num_heads, device):
+    """A uint8 device tensor sized for kda_prefill_ex on `device` (None when no workspace is used)."""
+    import torch
+    with torch.cuda.device(device):
+        n = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
+
+
 def kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound=0.0,
                gate_mode="lower_bound", stream=None):
     """T = 1 decode of ``rows`` tokens against ``state_pool`` (updated in place)."""
@@ -163,14 +213,19 @@ def kda_device_status(stream=None):
 
 
 def prefill(q, k, v, g_raw, beta, cu_seqlens, init_state=None, *, scale, lower_bound=0.0,
-            gate_mode="lower_bound", want_final=True, stream=None):
-    """Allocates ``out`` (and ``final_state``) and runs ``kda_prefill``; returns (out, final_state)."""
+            gate_mode="lower_bound", want_final=True, workspace=None, stream=None):
+    """Allocates ``out`` (and ``final_state``) and runs ``kda_prefill`` (``kda_prefill_ex`` when a
+    workspace is given); returns (out, final_state)."""
     import torch
     T, H, d = q.shape
     N = cu_seqlens.shape[0] - 1
     out = torch.empty_like(q)
     final = torch.empty(N, H, d, d, dtype=torch.float32, device=q.device) if want_final else None
-    kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final, scale, lower_bound, gate_mode, stream)
+    if workspace is None:
+        kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final, scale, lower_bound, gate_mode, stream)
+    else:
+        kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final, scale, lower_bound, gate_mode,
+                       workspace, stream)
     return out, final
 
 

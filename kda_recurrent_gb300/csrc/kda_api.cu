@@ -63,22 +63,33 @@ const char *kda_status_string(int status) {
     }
 }
 
-int kda_prefill(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,
-                const int32_t *cu_seqlens, const float *init_state, void *out, float *final_state,
-                int32_t num_seqs, int32_t total_tokens, int32_t num_heads, float scale,
-                float lower_bound, int32_t gate_mode, kda_stream_t stream) {
+namespace {
+
+int sm_count_of_current_device(int32_t *sms) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KDA_ERR_CUDA;
+    *sms = n;
+    return KDA_OK;
+}
+
+int prefill_common(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,
+                   const int32_t *cu_seqlens, const float *init_state, void *out, float *final_state,
+                   int32_t num_seqs, int32_t total_tokens, int32_t num_heads, float scale, float lower_bound,
+                   int32_t gate_mode, void *workspace, int64_t workspace_bytes, cudaStream_t stream) {
     if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
     if (!isfinite(scale) || !valid_gate(gate_mode, lower_bound)) return KDA_ERR_INVALID_ARG;
     if ((int64_t)total_tokens * num_heads * kHeadDim > (int64_t)1 << 40) return KDA_ERR_UNSUPPORTED;
-    if ((int64_t)num_seqs * num_heads > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * num_heads > 0x7fffffffLL / 64) return KDA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !g_raw || !beta || !out)) return KDA_ERR_INVALID_ARG;
     if (total_tokens == 0 && final_state == nullptr) return KDA_OK;
-    const void *p16[] = {q, k, v, g_raw, out, init_state, final_state};
+    const void *p16[] = {q, k, v, g_raw, out, init_state, final_state, workspace};
     for (const void *p : p16)
         if (p && !aligned(p, 16)) return KDA_ERR_MISALIGNED;
     if (!aligned(beta, 4) || !aligned(cu_seqlens, 4)) return KDA_ERR_MISALIGNED;
+    if (workspace != nullptr && workspace_bytes < 0) return KDA_ERR_INVALID_ARG;
 
     PrefillArgs a;
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -96,9 +107,53 @@ int kda_prefill(const void *q, const void *k, const void *v, const void *g_raw, 
     a.gate_mode = gate_mode;
     a.scale = scale;
     a.lower_bound = lower_bound;
+    a.wins = 1;
+    a.win_chunks = 0;
+    a.ws = nullptr;
+    if (workspace != nullptr) {
+        int32_t sms = 0;
+        const int st = sm_count_of_current_device(&sms);
+        if (st != KDA_OK) return st;
+        const WindowPlan plan = plan_windows(num_seqs, total_tokens, num_heads, sms);
+        if (plan.wins > 1) {
+            if (workspace_bytes < plan.ws_bytes) return KDA_ERR_INVALID_ARG;
+            a.wins = plan.wins;
+            a.win_chunks = plan.win_chunks;
+            a.ws = static_cast<float *>(workspace);
+        }
+    }
     cudaError_t e = device_status_ptr(&a.status);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    return from_cuda(launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_prefill_tc(a, stream));
+}
+
+}  // namespace
+
+int kda_prefill(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,
+                const int32_t *cu_seqlens, const float *init_state, void *out, float *final_state,
+                int32_t num_seqs, int32_t total_tokens, int32_t num_heads, float scale,
+                float lower_bound, int32_t gate_mode, kda_stream_t stream) {
+    return prefill_common(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, num_seqs, total_tokens,
+                          num_heads, scale, lower_bound, gate_mode, nullptr, 0,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kda_prefill_ex(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,
+                   const int32_t *cu_seqlens, const float *init_state, void *out, float *final_state,
+                   int32_t num_seqs, int32_t total_tokens, int32_t num_heads, float scale, float lower_bound,
+                   int32_t gate_mode, void *workspace, int64_t workspace_bytes, kda_stream_t stream) {
+    return prefill_common(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, num_seqs, total_tokens,
+                          num_heads, scale, lower_bound, gate_mode, workspace, workspace_bytes,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t sm_count) {
+    if (num_seqs < 0 || total_tokens < 0 || num_heads < 1 || sm_count < 0) return KDA_ERR_INVALID_ARG;
+    if (sm_count == 0) {
+        const int st = sm_count_of_current_device(&sm_count);
+        if (st != KDA_OK) return st;
+    }
+    return plan_windows(num_seqs, total_tokens, num_heads, sm_count).ws_bytes;
 }
 
 int kda_decode(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,

@@ -50,10 +50,23 @@ struct PrefillArgs {
     int32_t num_seqs, total_tokens, num_heads, gate_mode;
     float scale, lower_bound;
     DeviceStatus *status;
+    // Window schedule for short chain counts: each chain's chunks are cut into `wins`
+    // windows of `win_chunks` chunks (wins = 1: one window per chain). `ws` holds, per
+    // (chain, window), three FP32 128 x 128 slots: the window's start state, and the
+    // window's zero-start end state E and linear map M (S_end = M S_start + E).
+    int32_t wins, win_chunks;
+    float *ws;
 };
 
+// Window plan of a prefill call on a device with `sms` multiprocessors.
+struct WindowPlan {
+    int32_t wins, win_chunks;
+    int64_t ws_bytes;
+};
+WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t sms);
+constexpr int64_t kWindowSlotBytes = 3LL * 128 * 128 * 4;
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
-cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);  // windows when a.wins > 1
 
 }  // namespace kda

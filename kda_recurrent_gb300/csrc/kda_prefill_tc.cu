@@ -28,6 +28,8 @@
 // prefix); the off-diagonal block factors through the half boundary (both factors <= 1).
 // All mbarrier waits are bounded; on expiry the kernel records KDA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
+#include <algorithm>
+
 #include "kda_internal.cuh"
 #include "kda_mma.cuh"
 #include "kda_tc.cuh"
@@ -102,6 +104,21 @@ static_assert(sizeof(Bars) <= 128, "barrier block");
 
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named-barrier sync of `count` threads that also returns, identically to all of them,
+// whether `pred` held for any of them.
+__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // Bounded wait; on expiry records a timeout and raises the CTA's abort flag.
@@ -198,6 +215,7 @@ __device__ __forceinline__ void load_vb(const PrefillArgs &a, uint8_t *smem, int
 
 // ------------------------------------------------------------------ producers
 
+template <bool kPass1>
 __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int n, int h, int bos,
                               int eos, int nchunks) {
     const int ptid = threadIdx.x;  // 0 .. 255
@@ -329,12 +347,12 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 const float fl0 = before_anchor ? F0[ii] : P0[ii], fl1 = before_anchor ? F1[ii] : P1[ii];
                 const float fr0 = before_anchor ? S0[ii] : F0[ii], fr1 = before_anchor ? S1[ii] : F1[ii];
                 ok &= (fl0 < 3.0e38f) && (fl1 < 3.0e38f) && (fr0 < 3.0e38f) && (fr1 < 3.0e38f);
-                st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
+                if (!kPass1) st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
                 st_pair(pairKL, i * kRowB + ch, k0 * fl0, k1 * fl1);
                 st_pair(pairKR, i * kRowB + ch, k0 * fr0, k1 * fr1);
                 if (qt >= 2) {
                     const float fo0 = od0 * P0[ii], fo1 = od1 * P1[ii];
-                    st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
+                    if (!kPass1) st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
                     st_pair(pairKL, (16 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
                 } else {
                     const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
@@ -342,7 +360,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 }
                 const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
                 st_pair(kbar_s, i * kRowB + ch, k0 * fb0, k1 * fb1);
-                st_pair(qbar_s, i * kRowB + ch, q0 * fb0, q1 * fb1);
+                if (!kPass1) st_pair(qbar_s, i * kRowB + ch, q0 * fb0, q1 * fb1);
                 kr0[ii] = __uint_as_float(to_tf32(k0 * (S0[ii] * post0)));  // 2^(G_L - G_i)
                 kr1[ii] = __uint_as_float(to_tf32(k1 * (S1[ii] * post1)));
             }
@@ -368,6 +386,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
 
         // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5)
         if (warp < 6) {
+          if (!(kPass1 && warp < 3)) {  // the Mqk blocks are not needed by the window pass
             const int which = warp / 3;
             const int blk = warp % 3;
             const uint8_t *Lb = which ? pairKL : pairQ;
@@ -398,6 +417,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     }
                 }
             }
+          }
         } else {
             for (int idx = ptid - 192; idx < 256; idx += 64) {
                 const int i = idx >> 4, j = 16 + (idx & 15);
@@ -454,8 +474,8 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         }
         bar_named(kBarProd, kProdThreads);
 
-        // ---- 5. Q' = Qbar - Mqk Wk (-> stage W rows 32-63), Ov = Mqk Wv
-        {
+        // ---- 5. Q' = Qbar - Mqk Wk (-> stage W rows 32-63), Ov = Mqk Wv (output pass only)
+        if (!kPass1) {
             uint32_t am[2][2][4], amn[2][2][4];
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
@@ -530,7 +550,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         const int db = c & 1;
         if (c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status)) break;
         tc_fence_after();
-        {
+        if (!kPass1 || warp < 4) {
             const float *src = (warp < 4) ? wv_s : ov_s;
             const int quad = warp & 3;
             const int dv = 32 * quad + lane;
@@ -540,7 +560,9 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 v0[t] = src[t * kRowF + dv];
                 v1[t] = src[(16 + t) * kRowF + dv];
             }
-            const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + kColD1 + 64 * db + 32 * (warp >> 2);
+            // output pass: D1 = [Wv | Ov] (64 columns per buffer); window pass: D1 = Wv (32)
+            const uint32_t col = kPass1 ? kColD1 + 32 * db : kColD1 + 64 * db + 32 * (warp >> 2);
+            const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + col;
             tmem_st16(taddr, v0);
             tmem_st16(taddr + 16, v1);
             tmem_wait_st();
@@ -554,8 +576,8 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
 
 // ------------------------------------------------------------------ state warps
 
-__device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int chain, int h,
-                           int bos, int eos, int nchunks) {
+__device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int h, int bos, int eos,
+                           int nchunks, const float *init, float *fin_out) {
     const int stid = threadIdx.x - kProdThreads;  // 0 .. 127
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;
@@ -563,7 +585,6 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const bool mma_thread = (warp == kFirstStateWarp) && (lane == 0);
     uint8_t *const ost = smem + kOst;
-    const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
 
     // initial state -> S^T buffer 0 (lane = dv, column = dk)
 #pragma unroll 1
@@ -571,7 +592,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-            v[e] = a.init_state ? a.init_state[sbase + (size_t)(16 * j + e) * kHeadDim + dv] : 0.0f;
+            v[e] = init ? init[(16 * j + e) * kHeadDim + dv] : 0.0f;
         tmem_st16(tmem + lane_base + kColS + 16 * j, v);
     }
     tmem_wait_st();
@@ -652,15 +673,14 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                 *reinterpret_cast<uint4 *>(a.out + ((size_t)(t0 + row) * a.num_heads + h) * kHeadDim + vec * 8) = v4;
             }
         }
-        bar_named(kBarState, kStateThreads);
-        alive = B->abort == 0;
+        alive = !bar_any(kBarState, kStateThreads, B->abort != 0);
     }
 
-    // final state (after the last update has completed)
-    if (B->abort == 0) {
+    // final state (after the last update has completed); the abort decision is uniform
+    if (!bar_any(kBarState, kStateThreads, B->abort != 0)) {
         if (nchunks > 0 && !wait_or_abort(&B->g2, (nchunks - 1) & 1, B, a.status)) return;
         tc_fence_after();
-        if (a.final_state != nullptr) {
+        if (fin_out != nullptr) {
             const uint32_t fin = kColS + 128 * (nchunks & 1);
 #pragma unroll 1
             for (int j = 0; j < 8; ++j) {
@@ -668,27 +688,161 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                 tmem_ld16(tmem + lane_base + fin + 16 * j, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) a.final_state[sbase + (size_t)(16 * j + e) * kHeadDim + dv] = v[e];
+                for (int e = 0; e < 16; ++e) fin_out[(16 * j + e) * kHeadDim + dv] = v[e];
             }
         }
     }
 }
 
+// ------------------------------------------------------------------ window pass: state warps
+//
+// From a zero start the window's end state E is the S chain with V; the window's linear map M
+// (S_end = M S_start + E) is the same recurrence with V = 0 started from I, so both chains
+// share the producers' operands. TMEM: S^T [0,128), M^T [128,256) (lanes = dv resp. dk'),
+// D1 for S (= Wv^T + U^T) at [256 + 32b), D1 for M at [320 + 32b). The decay runs in place
+// after the projection has read the state.
+constexpr uint32_t kColM = 128;
+constexpr uint32_t kColD1M = 320;
+constexpr uint32_t kIdescN32 = instr_desc(2, 128, 32);  // tf32, M128 N32
+
+__device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int nchunks,
+                                 float *E_out, float *M_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3;
+    const int row = 32 * quad + lane;
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    const bool mma_thread = (warp == kFirstStateWarp) && (lane == 0);
+
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {
+        float z[16], id[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            z[e] = 0.0f;
+            id[e] = (16 * j + e == row) ? 1.0f : 0.0f;
+        }
+        tmem_st16(tmem + lane_base + kColS + 16 * j, z);
+        tmem_st16(tmem + lane_base + kColM + 16 * j, id);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    bar_named(kBarState, kStateThreads);
+    tc_fence_after();
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int ps = c & 1, db = c & 1;
+        const uint8_t *stage = smem + kStage0 + ps * kStageBytes;
+        if (!wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status)) break;
+        if (c >= 1 && !wait_or_abort(&B->g2, (c - 1) & 1, B, a.status)) break;
+        tc_fence_after();
+        if (mma_thread) {
+            const uint32_t wbase = smem_addr(stage + kStW);
+#pragma unroll
+            for (int s = 0; s < 16; ++s) {
+                const uint64_t bd = smem_desc_kmajor(wbase + 256 * s, 128, 4096);
+                mma_tf32_ts(tmem + kColD1 + 32 * db, tmem + kColS + 8 * s, bd, kIdescN32, true);
+                mma_tf32_ts(tmem + kColD1M + 32 * db, tmem + kColM + 8 * s, bd, kIdescN32, s > 0);
+            }
+            mma_commit(&B->g1);
+        }
+        __syncwarp();
+        if (!wait_or_abort(&B->g1, c & 1, B, a.status)) break;
+        tc_fence_after();
+        {
+            const float *dec = reinterpret_cast<const float *>(stage + kStDec);
+#pragma unroll 1
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t col = (j < 8 ? kColS : kColM) + 16 * (j & 7);
+                float v[16];
+                tmem_ld16(tmem + lane_base + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] *= dec[16 * (j & 7) + e];
+                tmem_st16(tmem + lane_base + col, v);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&B->oread[db]);
+        bar_named(kBarState, kStateThreads);
+        tc_fence_after();
+        if (mma_thread) {
+            const uint32_t kbase = smem_addr(stage + kStKr);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t bd = smem_desc_kmajor(kbase + 256 * s, 128, 1024);
+                mma_tf32_ts(tmem + kColS, tmem + kColD1 + 32 * db + 8 * s, bd, kIdescG2, true);
+                mma_tf32_ts(tmem + kColM, tmem + kColD1M + 32 * db + 8 * s, bd, kIdescG2, true);
+            }
+            mma_commit(&B->g2);
+            mma_commit(&B->g2s[ps]);
+        }
+        __syncwarp();
+        if (bar_any(kBarState, kStateThreads, B->abort != 0)) break;
+    }
+    if (bar_any(kBarState, kStateThreads, B->abort != 0)) return;
+    if (nchunks > 0 && !wait_or_abort(&B->g2, (nchunks - 1) & 1, B, a.status)) return;
+    tc_fence_after();
+    // E[dk][dv] from S^T (lane dv, column dk); M[dk][dk'] from M^T (lane dk', column dk)
+#pragma unroll 1
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t col = (j < 8 ? kColS : kColM) + 16 * (j & 7);
+        float *dst = j < 8 ? E_out : M_out;
+        float v[16];
+        tmem_ld16(tmem + lane_base + col, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dst[(16 * (j & 7) + e) * kHeadDim + row] = v[e];
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+struct WindowSpan {
+    int bos, eos, w, wins_seq;
+    bool live;
+};
+
+// Sequence bounds of chain `chain` (validated and clamped) and the span of window `w`.
+__device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, int w) {
+    int sb = a.cu_seqlens[n], se = a.cu_seqlens[n + 1];
+    if (sb < 0 || se < sb || se > a.total_tokens) {
+        if (threadIdx.x == 0 && w == 0 && (blockIdx.x % (a.num_heads * max(a.wins, 1))) < (unsigned)max(a.wins, 1))
+            report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
+        sb = min(max(sb, 0), a.total_tokens);
+        se = min(max(se, sb), a.total_tokens);
+    }
+    const int chunks = (se - sb + kChunk - 1) / kChunk;
+    const int lw = a.win_chunks > 0 ? a.win_chunks : max(chunks, 1);
+    WindowSpan sp;
+    sp.wins_seq = max(1, (chunks + lw - 1) / lw);
+    sp.w = w;
+    sp.bos = sb + kChunk * lw * w;
+    sp.eos = min(se, sp.bos + kChunk * lw);
+    sp.live = w < sp.wins_seq;
+    if (!sp.live) sp.bos = sp.eos = sb;
+    return sp;
+}
+
+__device__ __forceinline__ float *window_slot(const PrefillArgs &a, int chain, int w, int k) {
+    return a.ws + ((size_t)(chain * max(a.wins, 1) + w) * 3 + k) * (kHeadDim * kHeadDim);
+}
+
+template <bool kPass1>
 __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Bars *B = reinterpret_cast<Bars *>(smem + kBars);
     const int warp = threadIdx.x >> 5;
     const int H = a.num_heads;
-    const int chain = blockIdx.x;
+    const int W = max(a.wins, 1);
+    const int chain = blockIdx.x / W;
+    const int w = blockIdx.x - chain * W;
     const int n = chain / H;
     const int h = chain - n * H;
-
-    int bos = a.cu_seqlens[n], eos = a.cu_seqlens[n + 1];
-    if (bos < 0 || eos < bos || eos > a.total_tokens) {
-        if (threadIdx.x == 0 && h == 0) report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
-        bos = min(max(bos, 0), a.total_tokens);
-        eos = min(max(eos, bos), a.total_tokens);
-    }
+    const WindowSpan sp = window_span(a, n, w);
+    // The window pass covers every window but the last (its map is never needed).
+    if (kPass1 ? (w >= sp.wins_seq - 1) : !sp.live) return;
+    const int bos = sp.bos, eos = sp.eos;
     const int nchunks = (eos - bos + kChunk - 1) / kChunk;
 
     if (threadIdx.x == 0) {
@@ -713,9 +867,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     const uint32_t tmem = B->tmem_base;
 
     if (warp < kProducerWarps) {
-        producer_loop(a, smem, B, tmem, n, h, bos, eos, nchunks);
+        producer_loop<kPass1>(a, smem, B, tmem, n, h, bos, eos, nchunks);
     } else {
-        state_loop(a, smem, B, tmem, chain, h, bos, eos, nchunks);
+        if (kPass1) {
+            state_loop_pass1(a, smem, B, tmem, nchunks, window_slot(a, chain, w, 1), window_slot(a, chain, w, 2));
+        } else {
+            const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
+            const float *init = (w == 0) ? (a.init_state ? a.init_state + sbase : nullptr) : window_slot(a, chain, w, 0);
+            float *fin = (w == sp.wins_seq - 1 && a.final_state) ? a.final_state + sbase : nullptr;
+            state_loop(a, smem, B, tmem, h, bos, eos, nchunks, init, fin);
+        }
         if (B->abort != 0 && warp == kFirstStateWarp && (threadIdx.x & 31) == 0) {
             // drain any MMA still in flight before the tensor memory is released
             mma_commit(&B->g1);
@@ -729,20 +890,106 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     if (warp == kFirstStateWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-}  // namespace
+// ------------------------------------------------------------------ window carry
+//
+// S_start[w+1] = M_w S_start[w] + E_w for every window of a chain, in FP32 on CUDA cores.
+// The dv columns of S are independent, so each CTA carries 8 of them through all windows.
+constexpr int kCarryCols = 8;
+constexpr int kCarryThreads = 256;
 
-cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
+__global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const PrefillArgs a) {
+    __shared__ __align__(16) float S[kHeadDim][kCarryCols];
+    const int blocks = kHeadDim / kCarryCols;
+    const int chain = blockIdx.x / blocks;
+    const int c0 = (blockIdx.x - chain * blocks) * kCarryCols;
+    const int n = chain / a.num_heads;
+    const WindowSpan sp = window_span(a, n, 0);
+    if (sp.wins_seq <= 1) return;
+    const int tid = threadIdx.x;
+    const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
+    for (int idx = tid; idx < kHeadDim * kCarryCols; idx += kCarryThreads) {
+        const int i = idx / kCarryCols, cc = idx % kCarryCols;
+        S[i][cc] = a.init_state ? a.init_state[sbase + (size_t)i * kHeadDim + c0 + cc] : 0.0f;
+    }
+    __syncthreads();
+    const int i = tid >> 1;          // output row
+    const int cq = (tid & 1) * 4;    // four of the block's columns
+    for (int w = 0; w + 1 < sp.wins_seq; ++w) {
+        const float *M = window_slot(a, chain, w, 2) + (size_t)i * kHeadDim;
+        const float *E = window_slot(a, chain, w, 1) + (size_t)i * kHeadDim + c0 + cq;
+        float acc[4] = {E[0], E[1], E[2], E[3]};
+#pragma unroll 4
+        for (int j = 0; j < kHeadDim; j += 4) {
+            const float4 m4 = *reinterpret_cast<const float4 *>(M + j);
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(&S[j + jj][cq]);
+                acc[0] = fmaf(mv[jj], s4.x, acc[0]);
+                acc[1] = fmaf(mv[jj], s4.y, acc[1]);
+                acc[2] = fmaf(mv[jj], s4.z, acc[2]);
+                acc[3] = fmaf(mv[jj], s4.w, acc[3]);
+            }
+        }
+        __syncthreads();
+        *reinterpret_cast<float4 *>(&S[i][cq]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(window_slot(a, chain, w + 1, 0) + (size_t)i * kHeadDim + c0 + cq) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();
+    }
+}
+
+template <bool kPass1>
+cudaError_t configure_once() {
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+        e = cudaFuncSetAttribute(kda_prefill_tc_kernel<kPass1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+// Windows pay off only when the chains alone leave most of the GPU idle: each window
+// costs a window pass (about the price of the sequential chunk loop over its chunks) and
+// the FP32 carry; at least 3 windows of at least 4 chunks each are required.
+WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t sms) {
+    WindowPlan p = {1, 0, 0};
+    const int64_t chains = (int64_t)num_seqs * num_heads;
+    const int64_t max_chunks = ((int64_t)total_tokens + kChunk - 1) / kChunk;  // bound on any one sequence
+    constexpr int64_t kMinWindowChunks = 4;
+    if (chains <= 0 || sms <= 0 || chains * 3 > sms) return p;
+    int64_t wins = std::min<int64_t>(sms / chains, max_chunks / kMinWindowChunks);
+    if (wins < 3) return p;
+    const int64_t lw = (max_chunks + wins - 1) / wins;
+    wins = (max_chunks + lw - 1) / lw;
+    p.wins = (int32_t)wins;
+    p.win_chunks = (int32_t)lw;
+    p.ws_bytes = chains * wins * kWindowSlotBytes;
+    return p;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
+    cudaError_t e = configure_once<false>();
+    if (e != cudaSuccess) return e;
     const int64_t chains = (int64_t)a.num_seqs * a.num_heads;
-    kda_prefill_tc_kernel<<<(unsigned)chains, kThreadsTc, kSmemTc, stream>>>(a);
+    const int W = a.wins > 1 ? a.wins : 1;
+    if (W > 1) {
+        e = configure_once<true>();
+        if (e != cudaSuccess) return e;
+        kda_prefill_tc_kernel<true><<<(unsigned)(chains * W), kThreadsTc, kSmemTc, stream>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, 0, stream>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    kda_prefill_tc_kernel<false><<<(unsigned)(chains * W), kThreadsTc, kSmemTc, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -91,6 +91,12 @@ def test_prefill_rejects_bad_arguments_on_host(lib, over, expect):
     assert prefill_call(lib, **over) == expect
 
 
+def test_prefill_ex_rejects_misaligned_workspace_on_host(lib):
+    r = lib.kda_prefill_ex(A16, A16, A16, A16, A16, A16, None, A16, None, 1, 32, 2, 0.1, -5.0, 0, A16 + 8, 1 << 20,
+                           None)
+    assert r == K.KDA_ERR_MISALIGNED
+
+
 @pytest.mark.parametrize("over,expect", [
     (dict(H=0), K.KDA_ERR_INVALID_ARG),
     (dict(R=-1), K.KDA_ERR_INVALID_ARG),
@@ -127,3 +133,18 @@ def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         K.load()
+
+
+def test_window_plan_on_host(lib):
+    """kda_prefill_workspace_size with an explicit SM count is host arithmetic only."""
+    slot = 3 * 128 * 128 * 4
+    assert K.kda_prefill_workspace_size(1, 8192, 8, sm_count=152) == 8 * 19 * slot   # 8 chains x 19 windows
+    assert K.kda_prefill_workspace_size(1, 512, 8, sm_count=152) == 8 * 4 * slot     # 16 chunks: 4 windows of 4
+    assert K.kda_prefill_workspace_size(16, 25729, 32, sm_count=152) == 0            # 512 chains fill the GPU
+    assert K.kda_prefill_workspace_size(8, 131072, 96, sm_count=152) == 0
+    assert K.kda_prefill_workspace_size(1, 64, 1, sm_count=152) == 0                 # 2 chunks: no windows
+    assert K.kda_prefill_workspace_size(0, 0, 1, sm_count=152) == 0
+    with pytest.raises(K.KdaError):
+        K.kda_prefill_workspace_size(1, 100, 0, sm_count=152)
+    with pytest.raises(K.KdaError):
+        K.kda_prefill_workspace_size(1, 100, 1, sm_count=-1)

@@ -1,0 +1,112 @@
+"""GPU parity of the windowed (chunk-parallel) prefill schedule, kda_prefill_ex, against the
+FP64 oracle and against the sequential schedule.
+
+The window pass carries each window's linear map M through the same tcgen05 chain as the
+state; the slow-decay cases make the carried part of the state dominate, so an error in M,
+in the carry or in the window bookkeeping shows up there first.
+"""
+import pytest
+import torch
+
+import kda_recurrent_gb300 as K
+import kda_synth as S
+from helpers import assert_out_close, assert_state_close, oracle_prefill, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+SCALE = S.DEFAULT_SCALE
+
+
+def to_dev(inp):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def windowed(inp, *, lower_bound, gate_mode, init=True):
+    d = to_dev(inp)
+    N, T, H = d["cu_seqlens"].shape[0] - 1, d["q"].shape[0], d["q"].shape[1]
+    ws = K.prefill_workspace(N, T, H, DEV)
+    assert ws is not None, "this shape should take the windowed schedule"
+    out, fin = K.prefill(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], d["cu_seqlens"],
+                         d["init_state"] if init else None, scale=SCALE, lower_bound=lower_bound,
+                         gate_mode=gate_mode, workspace=ws)
+    st, detail = K.kda_device_status()
+    assert st == K.KDA_OK, (st, detail)
+    return out.cpu(), fin.cpu()
+
+
+def check(inp, *, lower_bound, gate_mode):
+    out, fin = windowed(inp, lower_bound=lower_bound, gate_mode=gate_mode)
+    ref_out, ref_fin = oracle_prefill(inp, scale=SCALE, lower_bound=lower_bound, gate_mode=gate_mode)
+    assert_out_close(out, ref_out)
+    assert_state_close(fin, ref_fin)
+
+
+def test_windowed_h8_t8192():
+    cfg = S.configs()["prefill_h8_t8192"]
+    check(S.config_inputs(cfg), lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
+
+
+def test_windowed_matches_sequential():
+    cfg = S.configs()["prefill_h8_t8192"]
+    inp = S.config_inputs(cfg)
+    out_w, fin_w = windowed(inp, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
+    d = to_dev(inp)
+    out_s, fin_s = K.prefill(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], d["cu_seqlens"], d["init_state"],
+                             scale=SCALE, lower_bound=cfg.lower_bound)
+    assert rel_l2(out_w, out_s.cpu()) < 5e-3
+    assert rel_l2(fin_w, fin_s.cpu()) < 1e-3
+
+
+@pytest.mark.parametrize("rate", [0.002, 0.03])
+def test_windowed_slow_decay_carries_the_state(rate):
+    """g = -rate * |a| per token: the state remembers thousands of tokens, so the start state
+    of late windows is mostly carried through the maps M of earlier windows."""
+    inp = S.prefill_inputs([3000], 2, seed=31, init_std=0.02)
+    inp["g_raw"] = (-rate * inp["g_raw"].float().abs()).to(torch.bfloat16)
+    check(inp, lower_bound=0.0, gate_mode="log_decay")
+
+
+def test_windowed_ragged_multi_sequence():
+    inp = S.prefill_inputs([1000, 37, 0, 2500, 130], 2, seed=32, init_std=0.02)
+    check(inp, lower_bound=0.0, gate_mode="softplus")
+
+
+def test_windowed_zero_init_and_in_place():
+    inp = to_dev(S.prefill_inputs([2048], 4, seed=33, init_std=0.02))
+    ws = K.prefill_workspace(1, 2048, 4, DEV)
+    args = dict(scale=SCALE, lower_bound=-5.0, gate_mode="lower_bound")
+    out_ref = torch.empty_like(inp["q"])
+    fin_ref = torch.empty_like(inp["init_state"])
+    K.kda_prefill_ex(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"], inp["init_state"],
+                     out_ref, fin_ref, workspace=ws, **args)
+    state = inp["init_state"].clone()
+    out = torch.empty_like(inp["q"])
+    K.kda_prefill_ex(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"], state, out, state,
+                     workspace=ws, **args)
+    assert torch.equal(out, out_ref) and torch.equal(state, fin_ref)
+    out0, fin0 = windowed({k: v.cpu() if isinstance(v, torch.Tensor) else v for k, v in inp.items()},
+                          lower_bound=-5.0, gate_mode="lower_bound", init=False)
+    ref_out, ref_fin = oracle_prefill({**{k: v.cpu() for k, v in inp.items() if k != "init_state"},
+                                       "init_state": None}, scale=SCALE, lower_bound=-5.0, gate_mode="lower_bound")
+    assert_out_close(out0, ref_out)
+    assert_state_close(fin0, ref_fin)
+
+
+def test_workspace_rules():
+    inp = to_dev(S.prefill_inputs([1024], 2, seed=34, init_std=None))
+    need = K.kda_prefill_workspace_size(1, 1024, 2)
+    assert need > 0
+    out = torch.empty_like(inp["q"])
+    small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(K.KdaError) as ei:
+        K.kda_prefill_ex(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"], None, out, None,
+                         SCALE, -5.0, workspace=small)
+    assert ei.value.status == K.KDA_ERR_INVALID_ARG
+    # no workspace: the sequential schedule, bitwise equal to kda_prefill
+    out_a, fin_a = K.prefill(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"], None,
+                             scale=SCALE, lower_bound=-5.0)
+    out_b = torch.empty_like(out_a)
+    fin_b = torch.empty_like(fin_a)
+    K.kda_prefill_ex(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"], None, out_b, fin_b,
+                     SCALE, -5.0, workspace=None)
+    assert torch.equal(out_a, out_b) and torch.equal(fin_a, fin_b)
