@@ -144,6 +144,33 @@ KDA_API int kda_prefill_ex(const void *q, const void *k, const void *v, const vo
                            void *workspace, int64_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_prefill_noalloc -- kda_prefill_ex for callers that cannot allocate device memory.
+ * The pages have no counterpart; this is a library convenience. Some callers cannot hand
+ * the library a workspace: code embedded in an application that owns every device
+ * allocation through its own pool and forbids raw cudaMalloc, or latency-critical paths
+ * where an allocation's synchronisation and cost are not acceptable. This call takes the
+ * same arguments as kda_prefill and runs the window schedule with its scratch in a
+ * fixed array of KDA_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library image. Every GPU
+ * that loads the library holds that array until the process exits. The call allocates
+ * nothing.
+ *   - The first call on a device looks up the array's device address (a CUDA runtime
+ *     query, once per device). Make that first call before any stream capture.
+ *   - All calls share the one array. Calls whose GPU work overlaps (other streams, other
+ *     host threads on the same device) race and must be serialised by the caller. Each
+ *     call writes every scratch byte it reads before reading it, so stale contents from
+ *     an earlier call never matter.
+ *   - A shape whose window plan needs more than KDA_NOALLOC_SCRATCH_BYTES returns
+ *     KDA_ERR_UNSUPPORTED. On GB300 (152 SMs) every plan fits (at most 29.2 MiB).
+ *   - Shapes that need no windows run the sequential schedule, as kda_prefill.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+KDA_API int kda_prefill_noalloc(const void *q, const void *k, const void *v, const void *g_raw,
+                                const float *beta, const int32_t *cu_seqlens, const float *init_state,
+                                void *out, float *final_state, int32_t num_seqs, int32_t total_tokens,
+                                int32_t num_heads, float scale, float lower_bound, int32_t gate_mode,
+                                kda_stream_t stream);
+
+/*
  * kda_decode -- one token per row (T = 1) against a slot-indexed state pool.
  *   q, k, g_raw  BF16 [rows, num_heads, 128]
  *   v            BF16 [rows, num_heads, 128]

@@ -35,8 +35,8 @@ STATE_DTYPES = {"f32": 0, "bf16": 1}
 HEAD_DIM = 128
 CHUNK = 32
 
-EXPORTED_SYMBOLS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_workspace_size", "kda_decode", "kda_status_string",
-                    "kda_device_status", "kda_abi_version")
+EXPORTED_SYMBOLS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_workspace_size", "kda_prefill_noalloc", "kda_decode",
+                    "kda_status_string", "kda_device_status", "kda_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,8 @@ def load(build_if_missing: bool = False):
                                            vp]
             lib.kda_prefill_workspace_size.restype = ctypes.c_int64
             lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
+            lib.kda_prefill_noalloc.restype = ctypes.c_int
+            lib.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
             lib.kda_decode.restype = ctypes.c_int
             lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -169,6 +171,29 @@ def kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_stat
                                _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_ex")
+
+
+def kda_prefill_noalloc(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, scale, lower_bound=0.0,
+                        gate_mode="lower_bound", stream=None):
+    """The window-scheduled prefill without a caller workspace, for callers that cannot allocate
+    device memory: the library's own fixed 32 MiB scratch array stands in for it. Calls share
+    that array, so calls that overlap on the GPU must be serialised (see include/kda.h)."""
+    import torch
+    T, H, d = q.shape
+    N = cu_seqlens.shape[0] - 1
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("out", out)):
+        _check(t, name, torch.bfloat16, (T, H, d), dev)
+    _check(beta, "beta", torch.float32, (T, H), dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    for name, t in (("init_state", init_state), ("final_state", final_state)):
+        if t is not None:
+            _check(t, name, torch.float32, (N, H, d, d), dev)
+    st = load().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
+                                    _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
+                                    float(lower_bound), _mode(gate_mode), _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_noalloc")
 
 
 def prefill_workspace(num_seqs, total_tokens, num_heads, device):
