@@ -17,7 +17,17 @@
 //
 // Slot offsets: one 64-bit base pointer per CTA, then 32-bit offsets inside the
 // slot (the PR #5551 lesson on 64-bit per-access arithmetic).
+//
+// Two schedules, chosen by the item count: few items take the register kernel above,
+// split by column blocks so the GPU still fills up; many items take the streaming
+// kernel, one persistent CTA per SM that keeps a ring of whole states in shared memory,
+// each moved in and out by bulk (TMA) copies, so the copy engines always have the next
+// items' states in flight while the current one is updated.
 #include "kda_internal.cuh"
+#include "kda_mma.cuh"
+#include "kda_tc.cuh"
+
+#include <algorithm>
 
 namespace kda {
 namespace {
@@ -182,6 +192,254 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
     }
 }
 
+// ------------------------------------------------------------------ streaming schedule
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+template <typename T>
+struct StreamShape {
+    static constexpr int kStages = sizeof(T) == 4 ? 3 : 6;  // 192 KiB of states in flight per SM
+    static constexpr uint32_t kItemBytes = kHeadDim * kHeadDim * sizeof(T);
+    static constexpr uint32_t kPiece = 16384;               // bytes per bulk copy
+    static constexpr uint32_t kTokBytes = 4 * kHeadDim * 2;  // the item's q, k, g_raw, v rows
+    static constexpr uint32_t kStageBytes = kItemBytes + kTokBytes;
+    static constexpr int VEC = StateVec<T>::kElems;
+    static constexpr int RPP = kDecodeThreads / (kHeadDim / VEC);
+    static constexpr int kRed = 2 * RPP * kHeadDim * 4;
+    static constexpr int kSmem = kStages * kStageBytes + kRed + 5 * kHeadDim * 4 + 2 * kStages * 8;
+};
+
+__device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kDecodeThreads) : "memory"); }
+
+// One CTA per SM: warps 0-7 update states; warp 8 (lane 0) moves them. Stage s is filled by
+// bulk copies that complete `full[s]`; the compute warps arrive on `done[s]` once the
+// updated state is back in the stage; the producer then stores it with a bulk copy and,
+// once that copy has read the stage, refills it with the state NS items ahead.
+template <typename T>
+__global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kernel(DecodeArgs a) {
+    using V = StateVec<T>;
+    using SS = StreamShape<T>;
+    constexpr int NS = SS::kStages;
+    constexpr int VEC = V::kElems;
+    constexpr int VPR = kHeadDim / VEC;
+    constexpr int RPP = SS::RPP;
+    constexpr int NPASS = kHeadDim / RPP;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *const stages = smem;
+    float *const s_red = reinterpret_cast<float *>(smem + NS * SS::kStageBytes);  // [2][RPP][128]
+    float *const s_k = s_red + 2 * RPP * kHeadDim;
+    float *const s_q = s_k + kHeadDim;
+    float *const s_decay = s_q + kHeadDim;
+    float *const s_u = s_decay + kHeadDim;
+    float *const s_qk = s_u + kHeadDim;
+    uint64_t *const full = reinterpret_cast<uint64_t *>(s_qk + kHeadDim);
+    uint64_t *const done = full + NS;
+
+    const int tid = threadIdx.x;
+    const int H = a.num_heads;
+    const int64_t items = (int64_t)a.rows * H;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    const int mine = items > first ? (int)((items - first + stride - 1) / stride) : 0;
+    if (tid == 0) {
+        for (int st = 0; st < NS; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&done[st], kDecodeThreads);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto slot_of = [&](int64_t item) -> int64_t {  // slot of an item, or -1 (padding / past the pool)
+        const int32_t slot = __ldg(a.slot_idx + (int)(item / H));
+        return (slot >= 0 && (int64_t)slot < a.num_slots) ? (int64_t)slot : -1;
+    };
+    auto state_ptr = [&](int64_t item, int64_t slot) -> uint8_t * {
+        const int h = (int)(item % H);
+        return reinterpret_cast<uint8_t *>(reinterpret_cast<T *>(a.state_pool) +
+                                           ((size_t)slot * (size_t)H + (size_t)h) * (kHeadDim * kHeadDim));
+    };
+
+    if (tid >= kDecodeThreads) {
+        // ---- producer warp
+        if (tid != kDecodeThreads) return;
+        auto issue = [&](int kk) {
+            const int st = kk % NS;
+            const int64_t item = first + (int64_t)kk * stride;
+            const int64_t slot = slot_of(item);
+            if (slot < 0) {
+                mbar_arrive(&full[st]);
+                return;
+            }
+            const uint8_t *src = state_ptr(item, slot);
+            uint8_t *dst = stages + st * SS::kStageBytes;
+            mbar_expect_tx(&full[st], SS::kStageBytes);
+#pragma unroll
+            for (uint32_t p = 0; p < SS::kItemBytes; p += SS::kPiece)
+                bulk_load(smem_addr(dst + p), src + p, SS::kPiece, &full[st]);
+            const size_t tok = (size_t)item * kHeadDim;
+            const __nv_bfloat16 *rows[4] = {a.q + tok, a.k + tok, a.g_raw + tok, a.v + tok};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                bulk_load(smem_addr(dst + SS::kItemBytes + t * kHeadDim * 2), rows[t], kHeadDim * 2, &full[st]);
+        };
+        for (int kk = 0; kk < NS && kk < mine; ++kk) issue(kk);
+        for (int j = 0; j < mine; ++j) {
+            const int st = j % NS;
+            if (!mbar_wait(&done[st], (uint32_t)(j / NS) & 1u)) {
+                report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+                break;
+            }
+            const int64_t item = first + (int64_t)j * stride;
+            const int64_t slot = slot_of(item);
+            if (slot >= 0) {
+                uint8_t *dst = state_ptr(item, slot);
+#pragma unroll
+                for (uint32_t p = 0; p < SS::kItemBytes; p += SS::kPiece)
+                    bulk_store(dst + p, smem_addr(stages + st * SS::kStageBytes + p), SS::kPiece);
+                bulk_commit();
+            }
+            if (j + NS < mine) {
+                bulk_wait_read_all();  // the stage's store has read it
+                issue(j + NS);
+            }
+        }
+        bulk_wait_all();
+        return;
+    }
+
+    // ---- compute warps
+    const int cg = tid % VPR, rg = tid / VPR;
+    int64_t slot_next = mine > 0 ? slot_of(first) : -1;
+    float beta_next = (mine > 0 && tid < kHeadDim) ? a.beta[first] : 0.0f;
+    for (int kk = 0; kk < mine; ++kk) {
+        const int st = kk % NS;
+        const int64_t item = first + (int64_t)kk * stride;
+        const int r = (int)(item / H);
+        const int64_t slot = slot_next;
+        const float beta_cur = beta_next;
+        if (kk + 1 < mine) {
+            slot_next = slot_of(item + stride);
+            if (tid < kHeadDim) beta_next = a.beta[item + stride];
+        }
+        const size_t tok = (size_t)item * kHeadDim;
+        if (!mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u)) {
+            report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+            break;
+        }
+        if (slot < 0) {
+            if (tid < kHeadDim) a.out[tok + tid] = __float2bfloat16_rn(0.0f);
+            const int32_t raw_slot = __ldg(a.slot_idx + r);
+            if (tid == 0 && (int64_t)raw_slot >= a.num_slots && item % H == 0)
+                report_error(a.status, KDA_ERR_DEVICE_INPUT, r);
+            mbar_arrive(&done[st]);
+            continue;
+        }
+        const uint8_t *trow8 = stages + st * SS::kStageBytes + SS::kItemBytes;
+        const __nv_bfloat16 *trow = reinterpret_cast<const __nv_bfloat16 *>(trow8);
+        compute_bar();  // the previous item's use of the shared vectors is over
+        if (tid < kHeadDim) {
+            const float av = __bfloat162float(trow[2 * kHeadDim + tid]);
+            s_decay[tid] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
+            s_k[tid] = __bfloat162float(trow[kHeadDim + tid]);
+            s_q[tid] = __bfloat162float(trow[tid]);
+        }
+        compute_bar();
+        if (tid < 32) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int i = tid; i < kHeadDim; i += 32) acc = fmaf(s_q[i], s_k[i], acc);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (tid == 0) *s_qk = acc;
+        }
+        T *S = reinterpret_cast<T *>(stages + st * SS::kStageBytes);
+        typename V::Raw raw[NPASS];
+#pragma unroll
+        for (int p = 0; p < NPASS; ++p)
+            raw[p] = *reinterpret_cast<const typename V::Raw *>(S + (rg + p * RPP) * kHeadDim + cg * VEC);
+        float stv[NPASS][VEC];
+        float wk[VEC], wq[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) wk[e] = wq[e] = 0.0f;
+#pragma unroll
+        for (int p = 0; p < NPASS; ++p) {
+            V::unpack(raw[p], stv[p]);
+            const int row = rg + p * RPP;
+            const float d = s_decay[row], kr = s_k[row], qr = s_q[row];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                stv[p][e] *= d;
+                wk[e] = fmaf(stv[p][e], kr, wk[e]);
+                wq[e] = fmaf(stv[p][e], qr, wq[e]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            s_red[(0 * RPP + rg) * kHeadDim + cg * VEC + e] = wk[e];
+            s_red[(1 * RPP + rg) * kHeadDim + cg * VEC + e] = wq[e];
+        }
+        compute_bar();
+        if (tid < kHeadDim) {
+            float w_k = 0.0f, w_q = 0.0f;
+#pragma unroll 8
+            for (int i = 0; i < RPP; ++i) {
+                w_k += s_red[(0 * RPP + i) * kHeadDim + tid];
+                w_q += s_red[(1 * RPP + i) * kHeadDim + tid];
+            }
+            const float u = beta_cur * (__bfloat162float(trow[3 * kHeadDim + tid]) - w_k);
+            s_u[tid] = u;
+            a.out[tok + tid] = __float2bfloat16_rn(a.scale * fmaf(*s_qk, u, w_q));
+        }
+        compute_bar();
+#pragma unroll
+        for (int p = 0; p < NPASS; ++p) {
+            const int row = rg + p * RPP;
+            const float kr = s_k[row];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) stv[p][e] = fmaf(kr, s_u[cg * VEC + e], stv[p][e]);
+            *reinterpret_cast<typename V::Raw *>(S + row * kHeadDim + cg * VEC) = V::pack(stv[p]);
+        }
+        fence_async_smem();
+        mbar_arrive(&done[st]);
+    }
+}
+
+template <typename T>
+cudaError_t launch_decode_stream(const DecodeArgs &a, cudaStream_t stream, int sms) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kda_decode_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 StreamShape<T>::kSmem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    const int64_t items = (int64_t)a.rows * a.num_heads;
+    const int grid = (int)std::min<int64_t>(items, sms);
+    kda_decode_stream_kernel<T><<<grid, kDecodeThreads + 32, StreamShape<T>::kSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename T, int JW>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
     const int64_t ctas = (int64_t)a.rows * a.num_heads * (kHeadDim / JW);
@@ -190,18 +448,30 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Column-block width: whole rows when there are enough items to fill the GPU
-// several times over, narrower blocks (more CTAs per item) when there are not.
+// Column-block width of the register schedule: whole rows when there are enough items to
+// fill the GPU several times over, narrower blocks (more CTAs per item) when there are not.
 int pick_decode_width(int64_t items) {
     if (items >= 1024) return 128;
     if (items >= 256) return 64;
     return 32;
 }
 
+// Items from which the streaming schedule takes over (several per SM, so its ring fills).
+constexpr int kStreamItemsPerSm = 4;
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
-    const int jw = pick_decode_width((int64_t)a.rows * a.num_heads);
+    const int64_t items = (int64_t)a.rows * a.num_heads;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (items >= (int64_t)kStreamItemsPerSm * sms) {
+        if (a.state_dtype == KDA_STATE_F32) return launch_decode_stream<float>(a, stream, sms);
+        return launch_decode_stream<__nv_bfloat16>(a, stream, sms);
+    }
+    const int jw = pick_decode_width(items);
     if (a.state_dtype == KDA_STATE_F32) {
         if (jw == 128) return launch_decode_t<float, 128>(a, stream);
         if (jw == 64) return launch_decode_t<float, 64>(a, stream);

@@ -89,3 +89,35 @@ def test_decode_matches_prefill_of_length_one():
                              lower_bound=-5.0)
     assert_out_close(out_d.cpu(), out_p.double().cpu())
     assert_state_close(pool[slots.long()].cpu(), fin_p.double().cpu(), tol=1e-3)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_decode_streaming_schedule_with_padding_rows(state_dtype):
+    """Enough items for the streaming (bulk-copy ring) schedule, with padding rows and a slot
+    past the pool mixed in: those rows give zero outputs and touch no state."""
+    rows, H, slots_n = 700, 2, 2048
+    pool = S.state_pool(slots_n, H, state_dtype, std=0.02, seed=12, device=DEV)
+    before = pool.clone()
+    inp = S.decode_inputs(rows, H, seed=12, device=DEV)
+    slots = S.slot_indices(rows, slots_n, seed=12, device=DEV)
+    slots[5] = -1
+    slots[300] = -7
+    slots[611] = slots_n + 3
+    K.kda_device_status()
+    out = K.decode(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], slots, pool, scale=SCALE,
+                   lower_bound=-5.0)
+    st, detail = K.kda_device_status()
+    assert st == K.KDA_ERR_DEVICE_INPUT and detail == 611
+    pad = torch.tensor([5, 300, 611], device=DEV)
+    assert torch.count_nonzero(out[pad]) == 0
+    live = torch.ones(rows, dtype=torch.bool, device=DEV)
+    live[pad] = False
+    sl = slots[live].long()
+    after_sel = pool[sl].clone()
+    restored = pool.clone()
+    restored[sl] = before[sl]
+    assert torch.equal(bits(restored), bits(before)), "a slot outside the live rows changed"
+    ref_out, ref_state, _ = oracle.decode(inp["q"][live], inp["k"][live], inp["v"][live], inp["g_raw"][live],
+                                          inp["beta"][live], before[sl].double().cpu(), scale=SCALE, lower_bound=-5.0)
+    assert_out_close(out[live].cpu(), ref_out)
+    assert_state_close(after_sel.cpu(), ref_state)
