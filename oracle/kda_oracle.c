@@ -246,18 +246,30 @@ int oracle_kda_prefill(const double *q, const double *k, const double *v, const 
 typedef struct {
     const double *q, *k, *v, *a, *beta;
     double *state, *out;
-    int32_t items, dk, dv, gate_mode;
-    double scale, lower_bound;
+    int32_t items, dk, dv, gate_mode, beta_logits;
+    double scale, lower_bound, norm_eps;
     int32_t next;
     pthread_mutex_t lock;
     int failed;
 } decode_job;
 
+/* x <- x / sqrt(sum x^2 + eps): the L2 normalisation a decode call may apply to q and k. */
+static void oracle_l2norm(double *x, const double *src, int n, double eps)
+{
+    double ss = 0.0;
+    int i;
+    for (i = 0; i < n; ++i)
+        ss += src[i] * src[i];
+    ss = 1.0 / sqrt(ss + eps);
+    for (i = 0; i < n; ++i)
+        x[i] = src[i] * ss;
+}
+
 static void *decode_worker(void *arg)
 {
     decode_job *job = (decode_job *)arg;
     const int dk = job->dk, dv = job->dv;
-    double *w = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *w = (double *)malloc(sizeof(double) * (size_t)(dv + 2 * dk));
     if (!w) {
         pthread_mutex_lock(&job->lock);
         job->failed = 1;
@@ -271,10 +283,22 @@ static void *decode_worker(void *arg)
         pthread_mutex_unlock(&job->lock);
         if (it >= job->items)
             break;
-        oracle_token_step(job->state + (size_t)it * dk * dv, job->q + (size_t)it * dk,
-                          job->k + (size_t)it * dk, job->v + (size_t)it * dv,
-                          job->a + (size_t)it * dk, job->beta[it], dk, dv, job->scale,
-                          job->lower_bound, job->gate_mode, job->out + (size_t)it * dv, w);
+        {
+            const double *qi = job->q + (size_t)it * dk, *ki = job->k + (size_t)it * dk;
+            double beta = job->beta[it];
+            double *qn = w + dv, *kn = w + dv + dk;
+            if (job->norm_eps >= 0.0) {
+                oracle_l2norm(qn, qi, dk, job->norm_eps);
+                oracle_l2norm(kn, ki, dk, job->norm_eps);
+                qi = qn;
+                ki = kn;
+            }
+            if (job->beta_logits)
+                beta = 1.0 / (1.0 + exp(-beta));
+            oracle_token_step(job->state + (size_t)it * dk * dv, qi, ki, job->v + (size_t)it * dv,
+                              job->a + (size_t)it * dk, beta, dk, dv, job->scale, job->lower_bound,
+                              job->gate_mode, job->out + (size_t)it * dv, w);
+        }
     }
     free(w);
     return NULL;
@@ -286,10 +310,30 @@ static void *decode_worker(void *arg)
  * state: [items, dk, dv], updated in place.  The slot indirection of a state
  * pool is the caller's gather/scatter.
  */
+int oracle_kda_decode_ex(const double *q, const double *k, const double *v, const double *a,
+                         const double *beta, int32_t items, int32_t dk, int32_t dv, double *state,
+                         double scale, double lower_bound, int32_t gate_mode, double norm_eps,
+                         int32_t beta_logits, double *out, int32_t threads);
+
 int oracle_kda_decode(const double *q, const double *k, const double *v, const double *a,
                       const double *beta, int32_t items, int32_t dk, int32_t dv, double *state,
                       double scale, double lower_bound, int32_t gate_mode, double *out,
                       int32_t threads)
+{
+    return oracle_kda_decode_ex(q, k, v, a, beta, items, dk, dv, state, scale, lower_bound, gate_mode,
+                                -1.0, 0, out, threads);
+}
+
+/*
+ * The same step with the two input options of a decode call (FlashInfer PR #5551, decode ABI:
+ * "norm_eps"; PR #5573 section 3: the kernel stages sigmoid(beta) itself):
+ *   norm_eps >= 0  q and k are first replaced by x / sqrt(sum x^2 + norm_eps)
+ *   beta_logits    beta holds logits b and the step uses sigmoid(b) = 1 / (1 + exp(-b))
+ */
+int oracle_kda_decode_ex(const double *q, const double *k, const double *v, const double *a,
+                         const double *beta, int32_t items, int32_t dk, int32_t dv, double *state,
+                         double scale, double lower_bound, int32_t gate_mode, double norm_eps,
+                         int32_t beta_logits, double *out, int32_t threads)
 {
     decode_job job;
     int rc;
@@ -313,6 +357,8 @@ int oracle_kda_decode(const double *q, const double *k, const double *v, const d
     job.gate_mode = gate_mode;
     job.scale = scale;
     job.lower_bound = lower_bound;
+    job.norm_eps = norm_eps;
+    job.beta_logits = beta_logits;
     pthread_mutex_init(&job.lock, NULL);
     threads = resolve_threads(threads, items);
     rc = run_pool(decode_worker, &job, threads);

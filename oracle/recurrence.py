@@ -62,6 +62,11 @@ def _load():
             lib.oracle_kda_decode.argtypes = [dp, dp, dp, dp, dp, ctypes.c_int32, ctypes.c_int32,
                                               ctypes.c_int32, dp, ctypes.c_double, ctypes.c_double,
                                               ctypes.c_int32, dp, ctypes.c_int32]
+            lib.oracle_kda_decode_ex.restype = ctypes.c_int
+            lib.oracle_kda_decode_ex.argtypes = [dp, dp, dp, dp, dp, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32, dp, ctypes.c_double, ctypes.c_double,
+                                                 ctypes.c_int32, ctypes.c_double, ctypes.c_int32, dp,
+                                                 ctypes.c_int32]
             lib.oracle_kda_gate.restype = ctypes.c_double
             lib.oracle_kda_gate.argtypes = [ctypes.c_double, ctypes.c_int32, ctypes.c_double]
             _lib = lib
@@ -133,12 +138,15 @@ def prefill(q, k, v, g_raw, beta, cu_seqlens, init_state=None, *, scale, lower_b
 
 
 def decode(q, k, v, g_raw, beta, state, *, scale, lower_bound=0.0, gate_mode="lower_bound",
-           threads=0):
+           norm_eps=None, beta_logits=False, threads=0):
     """T = 1 decode on gathered states, in FP64.
 
     Shapes: q, k, g_raw [R, H, dk]; v [R, H, dv]; beta [R, H]; state [R, H, dk, dv]
     (the pool rows already gathered by slot). Returns (out [R, H, dv],
     new_state [R, H, dk, dv], threads_used); the input ``state`` is not modified.
+    ``norm_eps`` (not None) first L2-normalises q and k as x / sqrt(sum x^2 + eps);
+    ``beta_logits`` reads beta as logits and applies the logistic function (the two input
+    options of the decode ABI in FlashInfer PR #5551 / #5573).
     """
     q, k, v, a, b = (_f64(t) for t in (q, k, v, g_raw, beta))
     R, H, dk = q.shape
@@ -147,9 +155,10 @@ def decode(q, k, v, g_raw, beta, state, *, scale, lower_bound=0.0, gate_mode="lo
     assert st.shape == (R, H, dk, dv)
     out = np.zeros((R, H, dv), dtype=np.float64)
     lib = _load()
-    rc = lib.oracle_kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), R * H, dk, dv, _ptr(st),
-                               float(scale), float(lower_bound), _mode(gate_mode), _ptr(out),
-                               int(threads))
+    rc = lib.oracle_kda_decode_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), R * H, dk, dv, _ptr(st),
+                                  float(scale), float(lower_bound), _mode(gate_mode),
+                                  -1.0 if norm_eps is None else float(norm_eps), int(bool(beta_logits)),
+                                  _ptr(out), int(threads))
     if rc < 0:
         raise RuntimeError(f"oracle_kda_decode failed with {rc}")
     return out, st, rc

@@ -302,3 +302,30 @@ def test_chunked_form_rejects_exclusive_prefix():
     o_c, s_c = chunked.prefill_chain(c["q"][:, 0], c["k"][:, 0], c["v"][:, 0], a_shift[:, 0], c["beta"][:, 0],
                                      c["s0"][0, 0], scale=0.3, lower_bound=-5.0)
     assert rel(o_c, out[:, 0]) > 1e-3
+
+
+# ---------------------------------------------------------------- decode input options
+
+def test_decode_qk_normalisation_is_scale_invariant():
+    """With in-step L2 normalisation, scaling q and k by positive factors changes nothing
+    (up to the eps term), and unit inputs are left as they are."""
+    c = make_case(0, 3, 16, 16, seed=16, lens=[1] * 5, unit_k=False)
+    args = dict(scale=0.3, lower_bound=-5.0)
+    o1, s1, _ = oracle.decode(c["q"], c["k"], c["v"], c["a"], c["beta"], c["s0"], norm_eps=0.0, **args)
+    o2, s2, _ = oracle.decode(7.5 * c["q"], 0.02 * c["k"], c["v"], c["a"], c["beta"], c["s0"], norm_eps=0.0, **args)
+    assert rel(o1, o2) < 1e-13 and rel(s1, s2) < 1e-13
+    qn = c["q"] / np.linalg.norm(c["q"], axis=-1, keepdims=True)
+    kn = c["k"] / np.linalg.norm(c["k"], axis=-1, keepdims=True)
+    o3, s3, _ = oracle.decode(qn, kn, c["v"], c["a"], c["beta"], c["s0"], **args)
+    assert rel(o1, o3) < 1e-13 and rel(s1, s3) < 1e-13
+    o4, _, _ = oracle.decode(c["q"], c["k"], c["v"], c["a"], c["beta"], c["s0"], **args)
+    assert rel(o1, o4) > 1e-3  # not normalising changes the result
+
+
+def test_decode_beta_logits_match_library_logistic():
+    c = make_case(0, 2, 16, 16, seed=17, lens=[1] * 4)
+    logits = RNG.standard_normal(c["beta"].shape) * 3
+    args = dict(scale=0.3, gate_mode="softplus")
+    o1, s1, _ = oracle.decode(c["q"], c["k"], c["v"], c["a"], logits, c["s0"], beta_logits=True, **args)
+    o2, s2, _ = oracle.decode(c["q"], c["k"], c["v"], c["a"], expit(logits), c["s0"], **args)
+    assert rel(o1, o2) < 1e-14 and rel(s1, s2) < 1e-14
