@@ -36,7 +36,9 @@ HEAD_DIM = 128
 CHUNK = 32
 
 EXPORTED_SYMBOLS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_workspace_size", "kda_prefill_noalloc", "kda_decode",
-                    "kda_status_string", "kda_device_status", "kda_abi_version")
+                    "kda_decode_ex", "kda_status_string", "kda_device_status", "kda_abi_version")
+KDA_DECODE_L2NORM_QK = 1
+KDA_DECODE_BETA_LOGITS = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +77,9 @@ def load(build_if_missing: bool = False):
             lib.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
             lib.kda_decode.restype = ctypes.c_int
             lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, vp]
+            lib.kda_decode_ex.restype = ctypes.c_int
+            lib.kda_decode_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, i32, f32,
+                                          vp]
             lib.kda_status_string.restype = ctypes.c_char_p
             lib.kda_status_string.argtypes = [ctypes.c_int]
             lib.kda_device_status.restype = ctypes.c_int
@@ -207,6 +212,13 @@ def prefill_workspace(num_seqs, total_tokens, num_heads, device):
 def kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound=0.0,
                gate_mode="lower_bound", stream=None):
     """T = 1 decode of ``rows`` tokens against ``state_pool`` (updated in place)."""
+    kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, 0, 0.0, stream,
+                  _name="kda_decode")
+
+
+def kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound=0.0,
+                  gate_mode="lower_bound", flags=0, norm_eps=0.0, stream=None, _name="kda_decode_ex"):
+    """kda_decode with input options: KDA_DECODE_L2NORM_QK (with ``norm_eps``), KDA_DECODE_BETA_LOGITS."""
     import torch
     R, H, d = q.shape
     dev = q.device
@@ -221,11 +233,15 @@ def kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bou
     else:
         raise TypeError("state_pool must be float32 or bfloat16")
     _check(state_pool, "state_pool", state_pool.dtype, (state_pool.shape[0], H, d, d), dev)
-    st = load().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(slot_idx), _ptr(state_pool),
-                           int(state_pool.shape[0]), sdt, _ptr(out), R, H, float(scale), float(lower_bound),
-                           _mode(gate_mode), _stream_handle(stream, dev))
+    lib = load()
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(slot_idx), _ptr(state_pool),
+            int(state_pool.shape[0]), sdt, _ptr(out), R, H, float(scale), float(lower_bound), _mode(gate_mode))
+    if _name == "kda_decode":
+        st = lib.kda_decode(*args, _stream_handle(stream, dev))
+    else:
+        st = lib.kda_decode_ex(*args, int(flags), float(norm_eps), _stream_handle(stream, dev))
     if st != KDA_OK:
-        raise KdaError(st, "kda_decode")
+        raise KdaError(st, _name)
 
 
 def kda_device_status(stream=None):
@@ -255,10 +271,14 @@ def prefill(q, k, v, g_raw, beta, cu_seqlens, init_state=None, *, scale, lower_b
 
 
 def decode(q, k, v, g_raw, beta, slot_idx, state_pool, *, scale, lower_bound=0.0, gate_mode="lower_bound",
-           stream=None):
-    """Allocates ``out`` and runs ``kda_decode`` (pool updated in place); returns out."""
+           flags=0, norm_eps=0.0, stream=None):
+    """Allocates ``out`` and runs ``kda_decode`` / ``kda_decode_ex`` (pool updated in place); returns out."""
     import torch
     out = torch.empty_like(q)
-    kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, stream)
+    if flags:
+        kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, flags, norm_eps,
+                      stream)
+    else:
+        kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, stream)
     del torch
     return out

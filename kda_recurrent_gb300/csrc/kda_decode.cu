@@ -78,6 +78,44 @@ struct StateVec<__nv_bfloat16> {
     }
 };
 
+struct TokenScalars {
+    float qk;  // q_n . k_n
+    float rq;  // q_n = rq q
+    float rk;  // k_n = rk k
+};
+
+// Every calling warp computes q.k and, when the call asks for it, the L2 normalisation
+// factors (sum x^2 + eps)^-1/2 of q and k from the token vectors in shared memory; each
+// warp reads the same 2 x 128 values, so no barrier is needed.
+__device__ __forceinline__ TokenScalars token_scalars(const float *s_q, const float *s_k, const DecodeArgs &a) {
+    const int lane = threadIdx.x & 31;
+    float qk = 0.0f, qq = 0.0f, kk = 0.0f;
+#pragma unroll
+    for (int i = lane; i < kHeadDim; i += 32) {
+        const float q = s_q[i], k = s_k[i];
+        qk = fmaf(q, k, qk);
+        qq = fmaf(q, q, qq);
+        kk = fmaf(k, k, kk);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        qk += __shfl_xor_sync(0xffffffffu, qk, o);
+        qq += __shfl_xor_sync(0xffffffffu, qq, o);
+        kk += __shfl_xor_sync(0xffffffffu, kk, o);
+    }
+    TokenScalars t;
+    const bool norm = (a.flags & KDA_DECODE_L2NORM_QK) != 0;
+    t.rq = norm ? rsqrtf(qq + a.norm_eps) : 1.0f;
+    t.rk = norm ? rsqrtf(kk + a.norm_eps) : 1.0f;
+    t.qk = qk * t.rq * t.rk;
+    return t;
+}
+
+// beta as given, or the logistic function of a logit.
+__device__ __forceinline__ float beta_of(float b, const DecodeArgs &a) {
+    return (a.flags & KDA_DECODE_BETA_LOGITS) ? 1.0f / (1.0f + expf(-b)) : b;
+}
+
 template <typename T, int JW>
 __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a) {
     using V = StateVec<T>;
@@ -92,7 +130,6 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
     __shared__ float s_k[kHeadDim], s_q[kHeadDim], s_decay[kHeadDim];
     __shared__ float s_red[2][RPP][JW];
     __shared__ float s_u[JW];
-    __shared__ float s_qk;
 
     const int tid = threadIdx.x;
     const int item = blockIdx.x / NSPLIT;
@@ -133,14 +170,7 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
         s_q[tid] = __bfloat162float(a.q[tok + tid]);
     }
     __syncthreads();
-    if (tid < 32) {
-        float acc = 0.0f;
-#pragma unroll
-        for (int i = tid; i < kHeadDim; i += 32) acc = fmaf(s_q[i], s_k[i], acc);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (tid == 0) s_qk = acc;
-    }
+    const TokenScalars ts = token_scalars(s_q, s_k, a);
 
     // 3. Decay in registers and this thread's partial (D S)^T k and (D S)^T q.
     float st[NPASS][VEC];
@@ -161,8 +191,8 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
     }
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-        s_red[0][rg][cg * VEC + e] = wk[e];
-        s_red[1][rg][cg * VEC + e] = wq[e];
+        s_red[0][rg][cg * VEC + e] = wk[e] * ts.rk;
+        s_red[1][rg][cg * VEC + e] = wq[e] * ts.rq;
     }
     __syncthreads();
 
@@ -174,9 +204,9 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
             w_k += s_red[0][i][tid];
             w_q += s_red[1][i][tid];
         }
-        const float u = a.beta[item] * (__bfloat162float(a.v[tok + j0 + tid]) - w_k);
+        const float u = beta_of(a.beta[item], a) * (__bfloat162float(a.v[tok + j0 + tid]) - w_k);
         s_u[tid] = u;
-        out[tid] = __float2bfloat16_rn(a.scale * fmaf(s_qk, u, w_q));
+        out[tid] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
     }
     __syncthreads();
 
@@ -184,7 +214,7 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
 #pragma unroll
     for (int p = 0; p < NPASS; ++p) {
         const int row = rg + p * RPP;
-        const float kk = s_k[row];
+        const float kk = s_k[row] * ts.rk;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) st[p][e] = fmaf(kk, s_u[cg * VEC + e], st[p][e]);
         const uint32_t off = (uint32_t)row * kHeadDim + (uint32_t)cg * VEC;
@@ -249,8 +279,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     float *const s_q = s_k + kHeadDim;
     float *const s_decay = s_q + kHeadDim;
     float *const s_u = s_decay + kHeadDim;
-    float *const s_qk = s_u + kHeadDim;
-    uint64_t *const full = reinterpret_cast<uint64_t *>(s_qk + kHeadDim);
+    uint64_t *const full = reinterpret_cast<uint64_t *>(s_u + 2 * kHeadDim);
     uint64_t *const done = full + NS;
 
     const int tid = threadIdx.x;
@@ -362,14 +391,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             s_q[tid] = __bfloat162float(trow[tid]);
         }
         compute_bar();
-        if (tid < 32) {
-            float acc = 0.0f;
-#pragma unroll
-            for (int i = tid; i < kHeadDim; i += 32) acc = fmaf(s_q[i], s_k[i], acc);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (tid == 0) *s_qk = acc;
-        }
+        const TokenScalars ts = token_scalars(s_q, s_k, a);
         T *S = reinterpret_cast<T *>(stages + st * SS::kStageBytes);
         typename V::Raw raw[NPASS];
 #pragma unroll
@@ -393,8 +415,8 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
         }
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            s_red[(0 * RPP + rg) * kHeadDim + cg * VEC + e] = wk[e];
-            s_red[(1 * RPP + rg) * kHeadDim + cg * VEC + e] = wq[e];
+            s_red[(0 * RPP + rg) * kHeadDim + cg * VEC + e] = wk[e] * ts.rk;
+            s_red[(1 * RPP + rg) * kHeadDim + cg * VEC + e] = wq[e] * ts.rq;
         }
         compute_bar();
         if (tid < kHeadDim) {
@@ -404,15 +426,15 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                 w_k += s_red[(0 * RPP + i) * kHeadDim + tid];
                 w_q += s_red[(1 * RPP + i) * kHeadDim + tid];
             }
-            const float u = beta_cur * (__bfloat162float(trow[3 * kHeadDim + tid]) - w_k);
+            const float u = beta_of(beta_cur, a) * (__bfloat162float(trow[3 * kHeadDim + tid]) - w_k);
             s_u[tid] = u;
-            a.out[tok + tid] = __float2bfloat16_rn(a.scale * fmaf(*s_qk, u, w_q));
+            a.out[tok + tid] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
         }
         compute_bar();
 #pragma unroll
         for (int p = 0; p < NPASS; ++p) {
             const int row = rg + p * RPP;
-            const float kr = s_k[row];
+            const float kr = s_k[row] * ts.rk;
 #pragma unroll
             for (int e = 0; e < VEC; ++e) stv[p][e] = fmaf(kr, s_u[cg * VEC + e], stv[p][e]);
             *reinterpret_cast<typename V::Raw *>(S + row * kHeadDim + cg * VEC) = V::pack(stv[p]);

@@ -38,6 +38,8 @@ struct DecodeArgs {
     int32_t rows, num_heads, gate_mode, state_dtype;
     float scale, lower_bound;
     DeviceStatus *status;
+    int32_t flags;   // KDA_DECODE_* input options
+    float norm_eps;  // with KDA_DECODE_L2NORM_QK
 };
 
 struct PrefillArgs {

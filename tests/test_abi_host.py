@@ -115,6 +115,15 @@ def test_decode_rejects_bad_arguments_on_host(lib, over, expect):
     assert decode_call(lib, **over) == expect
 
 
+@pytest.mark.parametrize("flags,eps,expect", [(4, 0.0, K.KDA_ERR_INVALID_ARG), (1, -1.0, K.KDA_ERR_INVALID_ARG),
+                                              (1, float("nan"), K.KDA_ERR_INVALID_ARG), (2, -1.0, K.KDA_OK),
+                                              (3, 1e-6, K.KDA_OK)])
+def test_decode_ex_flag_validation_on_host(lib, flags, eps, expect):
+    # rows = 0 makes valid calls a no-op that never touches the device
+    r = lib.kda_decode_ex(A16, A16, A16, A16, A16, A16, A16, 16, 0, A16, 0, 2, 0.1, -5.0, 0, flags, eps, None)
+    assert r == expect
+
+
 def test_binding_checks_dtypes_and_shapes_before_calling(lib):
     q = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
     beta = torch.zeros(4, 2)

@@ -121,3 +121,69 @@ def test_decode_streaming_schedule_with_padding_rows(state_dtype):
                                           inp["beta"][live], before[sl].double().cpu(), scale=SCALE, lower_bound=-5.0)
     assert_out_close(out[live].cpu(), ref_out)
     assert_state_close(after_sel.cpu(), ref_state)
+
+
+@pytest.mark.parametrize("rows", [5, 900])  # the register schedule and the streaming schedule
+@pytest.mark.parametrize("flags", [K.KDA_DECODE_L2NORM_QK, K.KDA_DECODE_BETA_LOGITS,
+                                   K.KDA_DECODE_L2NORM_QK | K.KDA_DECODE_BETA_LOGITS])
+def test_decode_input_options(rows, flags):
+    """Raw N(0,1) q, k (normalised in the kernel when asked) and beta given as N(0,1) logits."""
+    H = 2
+    gen = torch.Generator(device="cpu").manual_seed(40 + rows + flags)
+    q = torch.randn(rows, H, 128, generator=gen).to(torch.bfloat16)
+    k = torch.randn(rows, H, 128, generator=gen).to(torch.bfloat16)
+    if not flags & K.KDA_DECODE_L2NORM_QK:  # keep the state contractive without normalisation
+        q = (q.float() / 11.3).to(torch.bfloat16)
+        k = (k.float() / 11.3).to(torch.bfloat16)
+    v = torch.randn(rows, H, 128, generator=gen).to(torch.bfloat16)
+    g = torch.randn(rows, H, 128, generator=gen).to(torch.bfloat16)
+    b = torch.randn(rows, H, generator=gen)
+    if not flags & K.KDA_DECODE_BETA_LOGITS:
+        b = torch.sigmoid(b)
+    pool = S.state_pool(1024, H, "f32", std=0.02, seed=41, device=DEV)
+    slots = S.slot_indices(rows, 1024, seed=41, device=DEV)
+    before = pool[slots.long()].double().cpu()
+    out = K.decode(*(t.to(DEV) for t in (q, k, v, g, b)), slots, pool, scale=SCALE, lower_bound=-5.0, flags=flags,
+                   norm_eps=1e-6)
+    assert K.kda_device_status()[0] == K.KDA_OK
+    ref_out, ref_state, _ = oracle.decode(q, k, v, g, b, before, scale=SCALE, lower_bound=-5.0,
+                                          norm_eps=1e-6 if flags & K.KDA_DECODE_L2NORM_QK else None,
+                                          beta_logits=bool(flags & K.KDA_DECODE_BETA_LOGITS))
+    assert_out_close(out.cpu(), ref_out)
+    assert_state_close(pool[slots.long()].cpu(), ref_state)
+
+
+def test_decode_and_windowed_prefill_replay_in_a_cuda_graph():
+    """Captured once, replayed twice: the same bytes as eager calls on the same inputs."""
+    H, rows = 8, 700
+    d = S.decode_inputs(rows, H, seed=42, device=DEV)
+    slots = S.slot_indices(rows, 4096, seed=42, device=DEV)
+    pool0 = S.state_pool(4096, H, "f32", std=0.02, seed=42, device=DEV)
+    p = S.prefill_inputs([2048], 4, seed=43, init_std=0.02, device=DEV)
+    ws = K.prefill_workspace(1, 2048, 4, DEV)
+    out_p, fin_p = torch.empty_like(p["q"]), torch.empty_like(p["init_state"])
+    out_d = torch.empty_like(d["q"])
+
+    def step(pool):
+        K.kda_prefill_ex(p["q"], p["k"], p["v"], p["g_raw"], p["beta"], p["cu_seqlens"], p["init_state"], out_p,
+                         fin_p, SCALE, -5.0, workspace=ws)
+        K.kda_decode(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], slots, pool, out_d, SCALE, -5.0)
+
+    eager_pool = pool0.clone()
+    step(eager_pool)                      # first calls (one-time set-up) happen before capture
+    eager = (out_p.clone(), fin_p.clone(), out_d.clone(), eager_pool.clone())
+    graph_pool = pool0.clone()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=s):
+            step(graph_pool)
+    for _ in range(2):
+        graph_pool.copy_(pool0)
+        out_p.zero_(), fin_p.zero_(), out_d.zero_()
+        gph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_p, eager[0]) and torch.equal(fin_p, eager[1]) and torch.equal(out_d, eager[2])
+        assert torch.equal(graph_pool, eager[3])
+    assert K.kda_device_status()[0] == K.KDA_OK
