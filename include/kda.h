@@ -195,24 +195,31 @@ KDA_API int kda_decode(const void *q, const void *k, const void *v, const void *
                float lower_bound, int32_t gate_mode, kda_stream_t stream);
 
 /*
- * kda_decode_ex -- kda_decode with the decode ABI's input options (FlashInfer PR #5551:
- * the persistent_rows ABI passes norm_eps; PR #5573 section 3: the kernel applies the
+ * kda_decode_ex -- kda_decode with several tokens per row and the decode ABI's input
+ * options (FlashInfer PR #5551: the persistent_rows ABI passes norm_eps, and the packed
+ * decode routes T > 1 to a multi-token kernel; PR #5573 section 3: the kernel applies the
  * logistic function to beta itself).
- *   flags     bitwise OR of
- *               KDA_DECODE_L2NORM_QK    q and k are first replaced, in FP32, by
- *                                       x * (sum x^2 + norm_eps)^-1/2
- *               KDA_DECODE_BETA_LOGITS  beta holds logits b; the step uses 1 / (1 + e^-b)
- *             other bits give KDA_ERR_INVALID_ARG.
- *   norm_eps  used with KDA_DECODE_L2NORM_QK; must be finite and >= 0.
- * All other arguments as kda_decode (which is kda_decode_ex with flags = 0).
+ *   tokens_per_row  T in [1, KDA_DECODE_MAX_TOKENS]. Row r applies its T tokens in order to
+ *                   pool slot slot_idx[r] (read once, written once). q, k, g_raw, v and out
+ *                   are [rows, T, num_heads, 128]; beta is [rows, T, num_heads]. T = 1 is
+ *                   kda_decode's layout. Larger T gives KDA_ERR_UNSUPPORTED.
+ *   flags           bitwise OR of
+ *                     KDA_DECODE_L2NORM_QK    q and k are first replaced, in FP32, by
+ *                                             x * (sum x^2 + norm_eps)^-1/2
+ *                     KDA_DECODE_BETA_LOGITS  beta holds logits b; the step uses 1 / (1 + e^-b)
+ *                   other bits give KDA_ERR_INVALID_ARG.
+ *   norm_eps        used with KDA_DECODE_L2NORM_QK; must be finite and >= 0.
+ * All other arguments as kda_decode (which is kda_decode_ex with T = 1 and flags = 0).
  */
 #define KDA_DECODE_L2NORM_QK 1
 #define KDA_DECODE_BETA_LOGITS 2
+#define KDA_DECODE_MAX_TOKENS 16
 KDA_API int kda_decode_ex(const void *q, const void *k, const void *v, const void *g_raw,
                           const float *beta, const int32_t *slot_idx, void *state_pool,
                           int64_t num_slots, int32_t state_dtype, void *out, int32_t rows,
-                          int32_t num_heads, float scale, float lower_bound, int32_t gate_mode,
-                          int32_t flags, float norm_eps, kda_stream_t stream);
+                          int32_t tokens_per_row, int32_t num_heads, float scale,
+                          float lower_bound, int32_t gate_mode, int32_t flags, float norm_eps,
+                          kda_stream_t stream);
 
 /* A static, human-readable name for a kda_status value. Never NULL. */
 KDA_API const char *kda_status_string(int status);

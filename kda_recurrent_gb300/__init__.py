@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_workspace_size
                     "kda_decode_ex", "kda_status_string", "kda_device_status", "kda_abi_version")
 KDA_DECODE_L2NORM_QK = 1
 KDA_DECODE_BETA_LOGITS = 2
+KDA_DECODE_MAX_TOKENS = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -78,8 +79,8 @@ def load(build_if_missing: bool = False):
             lib.kda_decode.restype = ctypes.c_int
             lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, vp]
             lib.kda_decode_ex.restype = ctypes.c_int
-            lib.kda_decode_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, i32, f32,
-                                          vp]
+            lib.kda_decode_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, f32, f32, i32, i32,
+                                          f32, vp]
             lib.kda_status_string.restype = ctypes.c_char_p
             lib.kda_status_string.argtypes = [ctypes.c_int]
             lib.kda_device_status.restype = ctypes.c_int
@@ -212,19 +213,35 @@ def prefill_workspace(num_seqs, total_tokens, num_heads, device):
 def kda_decode(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound=0.0,
                gate_mode="lower_bound", stream=None):
     """T = 1 decode of ``rows`` tokens against ``state_pool`` (updated in place)."""
-    kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, 0, 0.0, stream,
-                  _name="kda_decode")
+    _decode_call("kda_decode", q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, 0,
+                 0.0, stream)
 
 
 def kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound=0.0,
-                  gate_mode="lower_bound", flags=0, norm_eps=0.0, stream=None, _name="kda_decode_ex"):
-    """kda_decode with input options: KDA_DECODE_L2NORM_QK (with ``norm_eps``), KDA_DECODE_BETA_LOGITS."""
+                  gate_mode="lower_bound", flags=0, norm_eps=0.0, stream=None):
+    """Decode with T tokens per row (q, k, v, g_raw, out [R, T, H, 128]; beta [R, T, H]; 3-D
+    tensors mean T = 1) and the input options KDA_DECODE_L2NORM_QK (with ``norm_eps``) and
+    KDA_DECODE_BETA_LOGITS."""
+    _decode_call("kda_decode_ex", q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode,
+                 flags, norm_eps, stream)
+
+
+def _decode_call(name, q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_bound, gate_mode, flags,
+                 norm_eps, stream):
     import torch
-    R, H, d = q.shape
+    if q.dim() == 3:
+        R, H, d = q.shape
+        T = 1
+        tok_shape, beta_shape = (R, H, d), (R, H)
+    else:
+        R, T, H, d = q.shape
+        tok_shape, beta_shape = (R, T, H, d), (R, T, H)
+        if name == "kda_decode":
+            raise ValueError("kda_decode takes one token per row; use kda_decode_ex")
     dev = q.device
-    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("out", out)):
-        _check(t, name, torch.bfloat16, (R, H, d), dev)
-    _check(beta, "beta", torch.float32, (R, H), dev)
+    for nm, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("out", out)):
+        _check(t, nm, torch.bfloat16, tok_shape, dev)
+    _check(beta, "beta", torch.float32, beta_shape, dev)
     _check(slot_idx, "slot_idx", torch.int32, (R,), dev)
     if state_pool.dtype == torch.float32:
         sdt = STATE_DTYPES["f32"]
@@ -234,14 +251,15 @@ def kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, lower_
         raise TypeError("state_pool must be float32 or bfloat16")
     _check(state_pool, "state_pool", state_pool.dtype, (state_pool.shape[0], H, d, d), dev)
     lib = load()
-    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(slot_idx), _ptr(state_pool),
-            int(state_pool.shape[0]), sdt, _ptr(out), R, H, float(scale), float(lower_bound), _mode(gate_mode))
-    if _name == "kda_decode":
-        st = lib.kda_decode(*args, _stream_handle(stream, dev))
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(slot_idx), _ptr(state_pool),
+            int(state_pool.shape[0]), sdt, _ptr(out), R)
+    tail = (float(scale), float(lower_bound), _mode(gate_mode))
+    if name == "kda_decode":
+        st = lib.kda_decode(*head, H, *tail, _stream_handle(stream, dev))
     else:
-        st = lib.kda_decode_ex(*args, int(flags), float(norm_eps), _stream_handle(stream, dev))
+        st = lib.kda_decode_ex(*head, T, H, *tail, int(flags), float(norm_eps), _stream_handle(stream, dev))
     if st != KDA_OK:
-        raise KdaError(st, _name)
+        raise KdaError(st, name)
 
 
 def kda_device_status(stream=None):

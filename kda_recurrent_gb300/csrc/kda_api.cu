@@ -158,14 +158,15 @@ int64_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32
 
 int kda_decode_ex(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,
                   const int32_t *slot_idx, void *state_pool, int64_t num_slots, int32_t state_dtype, void *out,
-                  int32_t rows, int32_t num_heads, float scale, float lower_bound, int32_t gate_mode,
-                  int32_t flags, float norm_eps, kda_stream_t stream) {
-    if (rows < 0 || num_heads < 1 || num_slots < 1) return KDA_ERR_INVALID_ARG;
+                  int32_t rows, int32_t tokens_per_row, int32_t num_heads, float scale, float lower_bound,
+                  int32_t gate_mode, int32_t flags, float norm_eps, kda_stream_t stream) {
+    if (rows < 0 || num_heads < 1 || num_slots < 1 || tokens_per_row < 1) return KDA_ERR_INVALID_ARG;
+    if (tokens_per_row > KDA_DECODE_MAX_TOKENS) return KDA_ERR_UNSUPPORTED;
     if (state_dtype != KDA_STATE_F32 && state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
     if (!isfinite(scale) || !valid_gate(gate_mode, lower_bound)) return KDA_ERR_INVALID_ARG;
     if ((flags & ~(KDA_DECODE_L2NORM_QK | KDA_DECODE_BETA_LOGITS)) != 0) return KDA_ERR_INVALID_ARG;
     if ((flags & KDA_DECODE_L2NORM_QK) && !(isfinite(norm_eps) && norm_eps >= 0.0f)) return KDA_ERR_INVALID_ARG;
-    if ((int64_t)rows * num_heads * 4 > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)rows * tokens_per_row * num_heads * 4 > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
     if (num_slots > ((int64_t)1 << 62) / ((int64_t)num_heads * kHeadDim * kHeadDim * 4))
         return KDA_ERR_UNSUPPORTED;
     if (rows == 0) return KDA_OK;
@@ -193,6 +194,7 @@ int kda_decode_ex(const void *q, const void *k, const void *v, const void *g_raw
     a.lower_bound = lower_bound;
     a.flags = flags;
     a.norm_eps = (flags & KDA_DECODE_L2NORM_QK) ? norm_eps : 0.0f;
+    a.tokens = tokens_per_row;
     cudaError_t e = device_status_ptr(&a.status);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     return from_cuda(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -202,8 +204,8 @@ int kda_decode(const void *q, const void *k, const void *v, const void *g_raw, c
                const int32_t *slot_idx, void *state_pool, int64_t num_slots, int32_t state_dtype,
                void *out, int32_t rows, int32_t num_heads, float scale, float lower_bound,
                int32_t gate_mode, kda_stream_t stream) {
-    return kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, num_slots, state_dtype, out, rows, num_heads,
-                         scale, lower_bound, gate_mode, 0, 0.0f, stream);
+    return kda_decode_ex(q, k, v, g_raw, beta, slot_idx, state_pool, num_slots, state_dtype, out, rows, 1,
+                         num_heads, scale, lower_bound, gate_mode, 0, 0.0f, stream);
 }
 
 int kda_device_status(kda_stream_t stream, int32_t *detail) {

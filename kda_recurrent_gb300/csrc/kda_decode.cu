@@ -244,17 +244,26 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
+// Shared-memory shape of the streaming schedule. A stage holds one item's state and the
+// q, k, g_raw, v rows of its `tokens` tokens; the stage count is whatever fits in
+// kStreamSmem (at most kMaxStages), so that 2-5 items are in flight per SM.
 template <typename T>
 struct StreamShape {
-    static constexpr int kStages = sizeof(T) == 4 ? 3 : 6;  // 192 KiB of states in flight per SM
+    static constexpr int kMaxStages = 6;
     static constexpr uint32_t kItemBytes = kHeadDim * kHeadDim * sizeof(T);
-    static constexpr uint32_t kPiece = 16384;               // bytes per bulk copy
-    static constexpr uint32_t kTokBytes = 4 * kHeadDim * 2;  // the item's q, k, g_raw, v rows
-    static constexpr uint32_t kStageBytes = kItemBytes + kTokBytes;
+    static constexpr uint32_t kPiece = 16384;               // bytes per bulk copy of the state
+    static constexpr uint32_t kTokBytes = 4 * kHeadDim * 2;  // q, k, g_raw, v rows of one token
     static constexpr int VEC = StateVec<T>::kElems;
     static constexpr int RPP = kDecodeThreads / (kHeadDim / VEC);
     static constexpr int kRed = 2 * RPP * kHeadDim * 4;
-    static constexpr int kSmem = kStages * kStageBytes + kRed + 5 * kHeadDim * 4 + 2 * kStages * 8;
+    static constexpr int kFixed = kRed + 4 * kHeadDim * 4 + kMaxTokensPerRow * 4 + 2 * kMaxStages * 8;
+    static constexpr int kStreamSmem = 220 * 1024;
+    static __host__ __device__ uint32_t stage_bytes(int tokens) { return kItemBytes + kTokBytes * tokens; }
+    static __host__ __device__ int stages(int tokens) {
+        const int n = (int)((kStreamSmem - kFixed) / stage_bytes(tokens));
+        return n < kMaxStages ? n : kMaxStages;
+    }
+    static __host__ __device__ int smem(int tokens) { return stages(tokens) * stage_bytes(tokens) + kFixed; }
 };
 
 __device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kDecodeThreads) : "memory"); }
@@ -262,25 +271,30 @@ __device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, %0;" :
 // One CTA per SM: warps 0-7 update states; warp 8 (lane 0) moves them. Stage s is filled by
 // bulk copies that complete `full[s]`; the compute warps arrive on `done[s]` once the
 // updated state is back in the stage; the producer then stores it with a bulk copy and,
-// once that copy has read the stage, refills it with the state NS items ahead.
+// once that copy has read the stage, refills it with the state NS items ahead. With
+// several tokens per row the state stays in registers while its tokens are applied in
+// order, and is stored once.
 template <typename T>
 __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kernel(DecodeArgs a) {
     using V = StateVec<T>;
     using SS = StreamShape<T>;
-    constexpr int NS = SS::kStages;
     constexpr int VEC = V::kElems;
     constexpr int VPR = kHeadDim / VEC;
     constexpr int RPP = SS::RPP;
     constexpr int NPASS = kHeadDim / RPP;
+    const int TT = a.tokens;
+    const int NS = SS::stages(TT);
+    const uint32_t stage_bytes = SS::stage_bytes(TT);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *const stages = smem;
-    float *const s_red = reinterpret_cast<float *>(smem + NS * SS::kStageBytes);  // [2][RPP][128]
+    float *const s_red = reinterpret_cast<float *>(smem + NS * stage_bytes);  // [2][RPP][128]
     float *const s_k = s_red + 2 * RPP * kHeadDim;
     float *const s_q = s_k + kHeadDim;
     float *const s_decay = s_q + kHeadDim;
     float *const s_u = s_decay + kHeadDim;
-    uint64_t *const full = reinterpret_cast<uint64_t *>(s_u + 2 * kHeadDim);
-    uint64_t *const done = full + NS;
+    float *const s_beta = s_u + kHeadDim;  // [kMaxTokensPerRow]
+    uint64_t *const full = reinterpret_cast<uint64_t *>(s_beta + kMaxTokensPerRow);
+    uint64_t *const done = full + SS::kMaxStages;
 
     const int tid = threadIdx.x;
     const int H = a.num_heads;
@@ -305,6 +319,11 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
         return reinterpret_cast<uint8_t *>(reinterpret_cast<T *>(a.state_pool) +
                                            ((size_t)slot * (size_t)H + (size_t)h) * (kHeadDim * kHeadDim));
     };
+    // element offset of the token rows / flat index of (item, token t): layout [rows][tokens][H]
+    auto tok_index = [&](int64_t item, int t) -> size_t {
+        const int64_t r = item / H, h = item % H;
+        return ((size_t)r * TT + t) * (size_t)H + (size_t)h;
+    };
 
     if (tid >= kDecodeThreads) {
         // ---- producer warp
@@ -318,16 +337,19 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                 return;
             }
             const uint8_t *src = state_ptr(item, slot);
-            uint8_t *dst = stages + st * SS::kStageBytes;
-            mbar_expect_tx(&full[st], SS::kStageBytes);
+            uint8_t *dst = stages + (size_t)st * stage_bytes;
+            mbar_expect_tx(&full[st], stage_bytes);
 #pragma unroll
             for (uint32_t p = 0; p < SS::kItemBytes; p += SS::kPiece)
                 bulk_load(smem_addr(dst + p), src + p, SS::kPiece, &full[st]);
-            const size_t tok = (size_t)item * kHeadDim;
-            const __nv_bfloat16 *rows[4] = {a.q + tok, a.k + tok, a.g_raw + tok, a.v + tok};
+            for (int t = 0; t < TT; ++t) {
+                const size_t tok = tok_index(item, t) * kHeadDim;
+                const __nv_bfloat16 *rows[4] = {a.q + tok, a.k + tok, a.g_raw + tok, a.v + tok};
+                uint8_t *tdst = dst + SS::kItemBytes + t * SS::kTokBytes;
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-                bulk_load(smem_addr(dst + SS::kItemBytes + t * kHeadDim * 2), rows[t], kHeadDim * 2, &full[st]);
+                for (int m = 0; m < 4; ++m)
+                    bulk_load(smem_addr(tdst + m * kHeadDim * 2), rows[m], kHeadDim * 2, &full[st]);
+            }
         };
         for (int kk = 0; kk < NS && kk < mine; ++kk) issue(kk);
         for (int j = 0; j < mine; ++j) {
@@ -342,7 +364,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                 uint8_t *dst = state_ptr(item, slot);
 #pragma unroll
                 for (uint32_t p = 0; p < SS::kItemBytes; p += SS::kPiece)
-                    bulk_store(dst + p, smem_addr(stages + st * SS::kStageBytes + p), SS::kPiece);
+                    bulk_store(dst + p, smem_addr(stages + (size_t)st * stage_bytes + p), SS::kPiece);
                 bulk_commit();
             }
             if (j + NS < mine) {
@@ -357,88 +379,95 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     // ---- compute warps
     const int cg = tid % VPR, rg = tid / VPR;
     int64_t slot_next = mine > 0 ? slot_of(first) : -1;
-    float beta_next = (mine > 0 && tid < kHeadDim) ? a.beta[first] : 0.0f;
+    float beta_next = (mine > 0 && tid < TT) ? a.beta[tok_index(first, tid)] : 0.0f;
     for (int kk = 0; kk < mine; ++kk) {
         const int st = kk % NS;
         const int64_t item = first + (int64_t)kk * stride;
         const int r = (int)(item / H);
         const int64_t slot = slot_next;
-        const float beta_cur = beta_next;
+        const float beta_mine = beta_next;  // beta of token `tid` of this item (tid < TT)
         if (kk + 1 < mine) {
             slot_next = slot_of(item + stride);
-            if (tid < kHeadDim) beta_next = a.beta[item + stride];
+            if (tid < TT) beta_next = a.beta[tok_index(item + stride, tid)];
         }
-        const size_t tok = (size_t)item * kHeadDim;
         if (!mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u)) {
             report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
             break;
         }
         if (slot < 0) {
-            if (tid < kHeadDim) a.out[tok + tid] = __float2bfloat16_rn(0.0f);
+            if (tid < kHeadDim)
+                for (int t = 0; t < TT; ++t) a.out[tok_index(item, t) * kHeadDim + tid] = __float2bfloat16_rn(0.0f);
             const int32_t raw_slot = __ldg(a.slot_idx + r);
             if (tid == 0 && (int64_t)raw_slot >= a.num_slots && item % H == 0)
                 report_error(a.status, KDA_ERR_DEVICE_INPUT, r);
             mbar_arrive(&done[st]);
             continue;
         }
-        const uint8_t *trow8 = stages + st * SS::kStageBytes + SS::kItemBytes;
-        const __nv_bfloat16 *trow = reinterpret_cast<const __nv_bfloat16 *>(trow8);
-        compute_bar();  // the previous item's use of the shared vectors is over
-        if (tid < kHeadDim) {
-            const float av = __bfloat162float(trow[2 * kHeadDim + tid]);
-            s_decay[tid] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
-            s_k[tid] = __bfloat162float(trow[kHeadDim + tid]);
-            s_q[tid] = __bfloat162float(trow[tid]);
-        }
-        compute_bar();
-        const TokenScalars ts = token_scalars(s_q, s_k, a);
-        T *S = reinterpret_cast<T *>(stages + st * SS::kStageBytes);
-        typename V::Raw raw[NPASS];
-#pragma unroll
-        for (int p = 0; p < NPASS; ++p)
-            raw[p] = *reinterpret_cast<const typename V::Raw *>(S + (rg + p * RPP) * kHeadDim + cg * VEC);
+        T *S = reinterpret_cast<T *>(stages + (size_t)st * stage_bytes);
         float stv[NPASS][VEC];
-        float wk[VEC], wq[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) wk[e] = wq[e] = 0.0f;
 #pragma unroll
         for (int p = 0; p < NPASS; ++p) {
-            V::unpack(raw[p], stv[p]);
-            const int row = rg + p * RPP;
-            const float d = s_decay[row], kr = s_k[row], qr = s_q[row];
+            const typename V::Raw raw =
+                *reinterpret_cast<const typename V::Raw *>(S + (rg + p * RPP) * kHeadDim + cg * VEC);
+            V::unpack(raw, stv[p]);
+        }
+        for (int t = 0; t < TT; ++t) {
+            const __nv_bfloat16 *trow =
+                reinterpret_cast<const __nv_bfloat16 *>(stages + (size_t)st * stage_bytes + SS::kItemBytes +
+                                                        t * SS::kTokBytes);
+            compute_bar();  // the previous step's use of the shared vectors is over
+            if (tid < kHeadDim) {
+                const float av = __bfloat162float(trow[2 * kHeadDim + tid]);
+                s_decay[tid] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
+                s_k[tid] = __bfloat162float(trow[kHeadDim + tid]);
+                s_q[tid] = __bfloat162float(trow[tid]);
+            }
+            if (t == 0 && tid < TT) s_beta[tid] = beta_mine;
+            compute_bar();
+            const TokenScalars ts = token_scalars(s_q, s_k, a);
+            float wk[VEC], wq[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) wk[e] = wq[e] = 0.0f;
+#pragma unroll
+            for (int p = 0; p < NPASS; ++p) {
+                const int row = rg + p * RPP;
+                const float d = s_decay[row], kr = s_k[row], qr = s_q[row];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    stv[p][e] *= d;
+                    wk[e] = fmaf(stv[p][e], kr, wk[e]);
+                    wq[e] = fmaf(stv[p][e], qr, wq[e]);
+                }
+            }
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                stv[p][e] *= d;
-                wk[e] = fmaf(stv[p][e], kr, wk[e]);
-                wq[e] = fmaf(stv[p][e], qr, wq[e]);
+                s_red[(0 * RPP + rg) * kHeadDim + cg * VEC + e] = wk[e] * ts.rk;
+                s_red[(1 * RPP + rg) * kHeadDim + cg * VEC + e] = wq[e] * ts.rq;
             }
-        }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            s_red[(0 * RPP + rg) * kHeadDim + cg * VEC + e] = wk[e] * ts.rk;
-            s_red[(1 * RPP + rg) * kHeadDim + cg * VEC + e] = wq[e] * ts.rq;
-        }
-        compute_bar();
-        if (tid < kHeadDim) {
-            float w_k = 0.0f, w_q = 0.0f;
+            compute_bar();
+            if (tid < kHeadDim) {
+                float w_k = 0.0f, w_q = 0.0f;
 #pragma unroll 8
-            for (int i = 0; i < RPP; ++i) {
-                w_k += s_red[(0 * RPP + i) * kHeadDim + tid];
-                w_q += s_red[(1 * RPP + i) * kHeadDim + tid];
+                for (int i = 0; i < RPP; ++i) {
+                    w_k += s_red[(0 * RPP + i) * kHeadDim + tid];
+                    w_q += s_red[(1 * RPP + i) * kHeadDim + tid];
+                }
+                const float u = beta_of(s_beta[t], a) * (__bfloat162float(trow[3 * kHeadDim + tid]) - w_k);
+                s_u[tid] = u;
+                a.out[tok_index(item, t) * kHeadDim + tid] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
             }
-            const float u = beta_of(beta_cur, a) * (__bfloat162float(trow[3 * kHeadDim + tid]) - w_k);
-            s_u[tid] = u;
-            a.out[tok + tid] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
-        }
-        compute_bar();
+            compute_bar();
 #pragma unroll
-        for (int p = 0; p < NPASS; ++p) {
-            const int row = rg + p * RPP;
-            const float kr = s_k[row] * ts.rk;
+            for (int p = 0; p < NPASS; ++p) {
+                const int row = rg + p * RPP;
+                const float kr = s_k[row] * ts.rk;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) stv[p][e] = fmaf(kr, s_u[cg * VEC + e], stv[p][e]);
-            *reinterpret_cast<typename V::Raw *>(S + row * kHeadDim + cg * VEC) = V::pack(stv[p]);
+                for (int e = 0; e < VEC; ++e) stv[p][e] = fmaf(kr, s_u[cg * VEC + e], stv[p][e]);
+            }
         }
+#pragma unroll
+        for (int p = 0; p < NPASS; ++p)
+            *reinterpret_cast<typename V::Raw *>(S + (rg + p * RPP) * kHeadDim + cg * VEC) = V::pack(stv[p]);
         fence_async_smem();
         mbar_arrive(&done[st]);
     }
@@ -452,13 +481,13 @@ cudaError_t launch_decode_stream(const DecodeArgs &a, cudaStream_t stream, int s
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
         e = cudaFuncSetAttribute(kda_decode_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 StreamShape<T>::kSmem);
+                                 StreamShape<T>::kStreamSmem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     const int64_t items = (int64_t)a.rows * a.num_heads;
     const int grid = (int)std::min<int64_t>(items, sms);
-    kda_decode_stream_kernel<T><<<grid, kDecodeThreads + 32, StreamShape<T>::kSmem, stream>>>(a);
+    kda_decode_stream_kernel<T><<<grid, kDecodeThreads + 32, StreamShape<T>::smem(a.tokens), stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -489,7 +518,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (items >= (int64_t)kStreamItemsPerSm * sms) {
+    if (a.tokens > 1 || items >= (int64_t)kStreamItemsPerSm * sms) {
         if (a.state_dtype == KDA_STATE_F32) return launch_decode_stream<float>(a, stream, sms);
         return launch_decode_stream<__nv_bfloat16>(a, stream, sms);
     }

@@ -11,6 +11,7 @@ namespace kda {
 
 constexpr int kHeadDim = KDA_HEAD_DIM;  // dk = dv = 128
 constexpr int kChunk = KDA_CHUNK;       // prefill chunk length
+constexpr int kMaxTokensPerRow = KDA_DECODE_MAX_TOKENS;
 
 // Device status word: [0] = first kda_status error code recorded, [1] = its detail.
 struct DeviceStatus {
@@ -40,6 +41,7 @@ struct DecodeArgs {
     DeviceStatus *status;
     int32_t flags;   // KDA_DECODE_* input options
     float norm_eps;  // with KDA_DECODE_L2NORM_QK
+    int32_t tokens;  // tokens per row (>= 1); token rows are laid out [rows][tokens][heads]
 };
 
 struct PrefillArgs {

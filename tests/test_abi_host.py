@@ -120,7 +120,14 @@ def test_decode_rejects_bad_arguments_on_host(lib, over, expect):
                                               (3, 1e-6, K.KDA_OK)])
 def test_decode_ex_flag_validation_on_host(lib, flags, eps, expect):
     # rows = 0 makes valid calls a no-op that never touches the device
-    r = lib.kda_decode_ex(A16, A16, A16, A16, A16, A16, A16, 16, 0, A16, 0, 2, 0.1, -5.0, 0, flags, eps, None)
+    r = lib.kda_decode_ex(A16, A16, A16, A16, A16, A16, A16, 16, 0, A16, 0, 1, 2, 0.1, -5.0, 0, flags, eps, None)
+    assert r == expect
+
+
+@pytest.mark.parametrize("tokens,expect", [(0, K.KDA_ERR_INVALID_ARG), (-2, K.KDA_ERR_INVALID_ARG),
+                                           (17, K.KDA_ERR_UNSUPPORTED), (16, K.KDA_OK), (1, K.KDA_OK)])
+def test_decode_tokens_per_row_validation_on_host(lib, tokens, expect):
+    r = lib.kda_decode_ex(A16, A16, A16, A16, A16, A16, A16, 16, 0, A16, 0, tokens, 2, 0.1, -5.0, 0, 0, 0.0, None)
     assert r == expect
 
 

@@ -187,3 +187,40 @@ def test_decode_and_windowed_prefill_replay_in_a_cuda_graph():
         assert torch.equal(out_p, eager[0]) and torch.equal(fin_p, eager[1]) and torch.equal(out_d, eager[2])
         assert torch.equal(graph_pool, eager[3])
     assert K.kda_device_status()[0] == K.KDA_OK
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,tokens", [(3, 2), (600, 2), (40, 5), (300, 16)])
+def test_multi_token_decode_equals_prefill_of_short_sequences(state_dtype, rows, tokens):
+    """T tokens per row applied in order to the row's slot: the oracle's prefill of T-token
+    sequences started from the gathered pool states. Row 1 is a padding row."""
+    H, slots_n = 2, 2048
+    p = S.prefill_inputs([tokens] * rows, H, seed=50 + rows + tokens, init_std=None)
+    shape4 = (rows, tokens, H, 128)
+    q, k, v, g = (p[n].reshape(shape4).contiguous() for n in ("q", "k", "v", "g_raw"))
+    beta = p["beta"].reshape(rows, tokens, H).contiguous()
+    pool = S.state_pool(slots_n, H, state_dtype, std=0.02, seed=51, device=DEV)
+    slots = S.slot_indices(rows, slots_n, seed=51, device=DEV)
+    if rows > 1:
+        slots[1] = -1
+    before = pool.clone()
+    out = torch.empty(shape4, dtype=torch.bfloat16, device=DEV)
+    K.kda_decode_ex(*(t.to(DEV) for t in (q, k, v, g, beta)), slots, pool, out, SCALE, -5.0)
+    assert K.kda_device_status()[0] == K.KDA_OK
+    live = torch.ones(rows, dtype=torch.bool)
+    if rows > 1:
+        live[1] = False
+        assert torch.count_nonzero(out[1]) == 0
+    sl = slots.cpu()[live].long()
+    init = before[sl.to(DEV)].double().cpu()
+    n_live = int(live.sum())
+    cu = torch.arange(0, (n_live + 1) * tokens, tokens, dtype=torch.int32)
+    flat = lambda t: t[live].reshape(n_live * tokens, H, *t.shape[3:]) if t.dim() == 4 else \
+        t[live].reshape(n_live * tokens, H)
+    ref_out, ref_fin, _ = oracle.prefill(flat(q), flat(k), flat(v), flat(g), flat(beta), cu, init, scale=SCALE,
+                                         lower_bound=-5.0)
+    assert_out_close(out.cpu()[live].reshape(n_live * tokens, H, 128), ref_out)
+    assert_state_close(pool[sl.to(DEV)].cpu(), ref_fin)
+    restored = pool.clone()
+    restored[sl.to(DEV)] = before[sl.to(DEV)]
+    assert torch.equal(bits(restored), bits(before)), "a slot outside the live rows changed"
