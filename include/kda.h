@@ -131,6 +131,13 @@ KDA_API int64_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_token
  * from a zero start, each window's end state E and linear map M (S_end = M S_start + E);
  * an FP32 carry pass walks the windows of each chain; the output pass then reruns every
  * window from its true start state. Results match kda_prefill up to rounding.
+ *   checkpoints      FP32 [ckpt_rows, num_heads, 128, 128] intermediate states, or NULL with
+ *                    ckpt_every = 0 (the FP32 checkpoint rows every 64 tokens of FlashInfer PR
+ *                    #5565, "1. Kernel body"): with ckpt_every > 0 (a multiple of 32), the state
+ *                    after the first (j + 1) * ckpt_every tokens of sequence n, for
+ *                    j = 0 .. T_n / ckpt_every - 1, is written to row ckpt_offsets[n] + j.
+ *   ckpt_offsets     int32 [num_seqs], device: first checkpoint row of each sequence. A row
+ *                    outside [0, ckpt_rows) is skipped and recorded as KDA_ERR_DEVICE_INPUT.
  *   workspace        NULL: the sequential schedule (same as kda_prefill);
  *                    otherwise at least kda_prefill_workspace_size(..., 0) bytes on the
  *                    current device, or KDA_ERR_INVALID_ARG. Its contents on entry do not
@@ -141,7 +148,9 @@ KDA_API int kda_prefill_ex(const void *q, const void *k, const void *v, const vo
                            const float *beta, const int32_t *cu_seqlens, const float *init_state,
                            void *out, float *final_state, int32_t num_seqs, int32_t total_tokens,
                            int32_t num_heads, float scale, float lower_bound, int32_t gate_mode,
-                           void *workspace, int64_t workspace_bytes, kda_stream_t stream);
+                           float *checkpoints, const int32_t *ckpt_offsets, int64_t ckpt_rows,
+                           int32_t ckpt_every, void *workspace, int64_t workspace_bytes,
+                           kda_stream_t stream);
 
 /*
  * kda_prefill_noalloc -- kda_prefill_ex for callers that cannot allocate device memory.

@@ -70,8 +70,8 @@ def load(build_if_missing: bool = False):
             lib.kda_prefill.restype = ctypes.c_int
             lib.kda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
             lib.kda_prefill_ex.restype = ctypes.c_int
-            lib.kda_prefill_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp, i64,
-                                           vp]
+            lib.kda_prefill_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp, vp,
+                                           i64, i32, vp, i64, vp]
             lib.kda_prefill_workspace_size.restype = ctypes.c_int64
             lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
             lib.kda_prefill_noalloc.restype = ctypes.c_int
@@ -153,8 +153,11 @@ def kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, sm_count=0) ->
 
 
 def kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, scale, lower_bound=0.0,
-                   gate_mode="lower_bound", workspace=None, stream=None):
-    """kda_prefill with a caller-owned device workspace (a uint8 tensor, or None)."""
+                   gate_mode="lower_bound", workspace=None, stream=None, checkpoints=None, ckpt_offsets=None,
+                   ckpt_every=0):
+    """kda_prefill with a caller-owned device workspace (a uint8 tensor, or None) and optional
+    intermediate states every ``ckpt_every`` tokens into ``checkpoints`` [rows, H, 128, 128] at
+    rows ``ckpt_offsets[n] + j``."""
     import torch
     T, H, d = q.shape
     N = cu_seqlens.shape[0] - 1
@@ -166,6 +169,9 @@ def kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_stat
     for name, t in (("init_state", init_state), ("final_state", final_state)):
         if t is not None:
             _check(t, name, torch.float32, (N, H, d, d), dev)
+    if ckpt_every:
+        _check(ckpt_offsets, "ckpt_offsets", torch.int32, (N,), dev)
+        _check(checkpoints, "checkpoints", torch.float32, (checkpoints.shape[0], H, d, d), dev)
     nbytes = 0
     if workspace is not None:
         if workspace.device != dev or not workspace.is_contiguous():
@@ -173,8 +179,10 @@ def kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_stat
         nbytes = workspace.numel() * workspace.element_size()
     st = load().kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
                                _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
-                               float(lower_bound), _mode(gate_mode), _ptr(workspace), nbytes,
-                               _stream_handle(stream, dev))
+                               float(lower_bound), _mode(gate_mode), _ptr(checkpoints if ckpt_every else None),
+                               _ptr(ckpt_offsets if ckpt_every else None),
+                               int(checkpoints.shape[0]) if ckpt_every else 0, int(ckpt_every), _ptr(workspace),
+                               nbytes, _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_ex")
 

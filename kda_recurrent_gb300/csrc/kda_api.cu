@@ -76,7 +76,8 @@ int sm_count_of_current_device(int32_t *sms) {
 int prefill_common(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,
                    const int32_t *cu_seqlens, const float *init_state, void *out, float *final_state,
                    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, float scale, float lower_bound,
-                   int32_t gate_mode, void *workspace, int64_t workspace_bytes, cudaStream_t stream) {
+                   int32_t gate_mode, float *ckpt, const int32_t *ckpt_offsets, int64_t ckpt_rows,
+                   int32_t ckpt_every, void *workspace, int64_t workspace_bytes, cudaStream_t stream) {
     if (num_seqs < 0 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARG;
     if (!isfinite(scale) || !valid_gate(gate_mode, lower_bound)) return KDA_ERR_INVALID_ARG;
     if ((int64_t)total_tokens * num_heads * kHeadDim > (int64_t)1 << 40) return KDA_ERR_UNSUPPORTED;
@@ -90,6 +91,11 @@ int prefill_common(const void *q, const void *k, const void *v, const void *g_ra
         if (p && !aligned(p, 16)) return KDA_ERR_MISALIGNED;
     if (!aligned(beta, 4) || !aligned(cu_seqlens, 4)) return KDA_ERR_MISALIGNED;
     if (workspace != nullptr && workspace_bytes < 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_every < 0 || ckpt_every % kChunk != 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_every > 0) {
+        if (!ckpt || !ckpt_offsets || ckpt_rows < 1) return KDA_ERR_INVALID_ARG;
+        if (!aligned(ckpt, 16) || !aligned(ckpt_offsets, 4)) return KDA_ERR_MISALIGNED;
+    }
 
     PrefillArgs a;
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -110,6 +116,10 @@ int prefill_common(const void *q, const void *k, const void *v, const void *g_ra
     a.wins = 1;
     a.win_chunks = 0;
     a.ws = nullptr;
+    a.ckpt = ckpt_every > 0 ? ckpt : nullptr;
+    a.ckpt_offsets = ckpt_every > 0 ? ckpt_offsets : nullptr;
+    a.ckpt_rows = ckpt_every > 0 ? ckpt_rows : 0;
+    a.ckpt_every = ckpt_every;
     if (workspace != nullptr) {
         int32_t sms = 0;
         const int st = sm_count_of_current_device(&sms);
@@ -134,17 +144,18 @@ int kda_prefill(const void *q, const void *k, const void *v, const void *g_raw, 
                 int32_t num_seqs, int32_t total_tokens, int32_t num_heads, float scale,
                 float lower_bound, int32_t gate_mode, kda_stream_t stream) {
     return prefill_common(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, num_seqs, total_tokens,
-                          num_heads, scale, lower_bound, gate_mode, nullptr, 0,
+                          num_heads, scale, lower_bound, gate_mode, nullptr, nullptr, 0, 0, nullptr, 0,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kda_prefill_ex(const void *q, const void *k, const void *v, const void *g_raw, const float *beta,
                    const int32_t *cu_seqlens, const float *init_state, void *out, float *final_state,
                    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, float scale, float lower_bound,
-                   int32_t gate_mode, void *workspace, int64_t workspace_bytes, kda_stream_t stream) {
+                   int32_t gate_mode, float *checkpoints, const int32_t *ckpt_offsets, int64_t ckpt_rows,
+                   int32_t ckpt_every, void *workspace, int64_t workspace_bytes, kda_stream_t stream) {
     return prefill_common(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, num_seqs, total_tokens,
-                          num_heads, scale, lower_bound, gate_mode, workspace, workspace_bytes,
-                          reinterpret_cast<cudaStream_t>(stream));
+                          num_heads, scale, lower_bound, gate_mode, checkpoints, ckpt_offsets, ckpt_rows, ckpt_every,
+                          workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int64_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t sm_count) {

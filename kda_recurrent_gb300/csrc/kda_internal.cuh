@@ -60,6 +60,13 @@ struct PrefillArgs {
     // window's zero-start end state E and linear map M (S_end = M S_start + E).
     int32_t wins, win_chunks;
     float *ws;
+    // Optional intermediate states: every `ckpt_every` tokens (a multiple of the chunk),
+    // the state after (j+1) * ckpt_every tokens of sequence n goes to row
+    // ckpt_offsets[n] + j of ckpt [ckpt_rows][H][128][128] (ckpt_every = 0: none).
+    float *ckpt;
+    const int32_t *ckpt_offsets;
+    int64_t ckpt_rows;
+    int32_t ckpt_every;
 };
 
 // Window plan of a prefill call on a device with `sms` multiprocessors.

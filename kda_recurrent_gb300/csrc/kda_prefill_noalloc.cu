@@ -62,6 +62,6 @@ extern "C" int kda_prefill_noalloc(const void *q, const void *k, const void *v, 
     const int st = kda::noalloc_scratch(&scratch);
     if (st != KDA_OK) return st;
     return kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, num_seqs, total_tokens,
-                          num_heads, scale, lower_bound, gate_mode, scratch, (int64_t)KDA_NOALLOC_SCRATCH_BYTES,
-                          stream);
+                          num_heads, scale, lower_bound, gate_mode, nullptr, nullptr, 0, 0, scratch,
+                          (int64_t)KDA_NOALLOC_SCRATCH_BYTES, stream);
 }

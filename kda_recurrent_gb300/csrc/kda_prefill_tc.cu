@@ -576,8 +576,34 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
 
 // ------------------------------------------------------------------ state warps
 
-__device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int h, int bos, int eos,
-                           int nchunks, const float *init, float *fin_out) {
+// Checkpoint row of the state after chunk `cg` (0-based within the sequence), or -1 when
+// that chunk does not end a checkpoint interval or the row lies past the buffer.
+__device__ __forceinline__ int64_t checkpoint_row(const PrefillArgs &a, int n, int cg, bool full_chunk) {
+    if (a.ckpt_every <= 0 || !full_chunk) return -1;
+    const int64_t end = (int64_t)(cg + 1) * kChunk;
+    if (end % a.ckpt_every != 0) return -1;
+    const int64_t row = (int64_t)a.ckpt_offsets[n] + end / a.ckpt_every - 1;
+    if (row < 0 || row >= a.ckpt_rows) {
+        if ((threadIdx.x & 127) == 0) report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
+        return -1;
+    }
+    return row;
+}
+
+// S (TMEM columns [col, col + 128), lane = dv) -> FP32 [dk][dv] at dst.
+__device__ __forceinline__ void store_state(uint32_t tmem_state, uint32_t lane_base, int dv, float *dst) {
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {
+        float v[16];
+        tmem_ld16(tmem_state + lane_base + 16 * j, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dst[(16 * j + e) * kHeadDim + dv] = v[e];
+    }
+}
+
+__device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int n, int h, int bos,
+                           int eos, int nchunks, int chunk_base, const float *init, float *fin_out) {
     const int stid = threadIdx.x - kProdThreads;  // 0 .. 127
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;
@@ -617,6 +643,12 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
             mma_commit(&B->g1);
         }
         __syncwarp();
+        if (c >= 1) {  // checkpoint of the state after chunk c-1 (read alongside the projection)
+            const int64_t row = checkpoint_row(a, n, chunk_base + c - 1, true);
+            if (row >= 0)
+                store_state(tmem + cur, lane_base, dv,
+                            a.ckpt + ((size_t)row * a.num_heads + h) * (kHeadDim * kHeadDim));
+        }
         // decay into the other state buffer while the projection reads this one
         {
             const float *dec = reinterpret_cast<const float *>(stage + kStDec);
@@ -680,6 +712,13 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
     if (!bar_any(kBarState, kStateThreads, B->abort != 0)) {
         if (nchunks > 0 && !wait_or_abort(&B->g2, (nchunks - 1) & 1, B, a.status)) return;
         tc_fence_after();
+        if (nchunks > 0) {
+            const bool full = bos + kChunk * nchunks <= eos;
+            const int64_t row = checkpoint_row(a, n, chunk_base + nchunks - 1, full);
+            if (row >= 0)
+                store_state(tmem + kColS + 128 * (nchunks & 1), lane_base, dv,
+                            a.ckpt + ((size_t)row * a.num_heads + h) * (kHeadDim * kHeadDim));
+        }
         if (fin_out != nullptr) {
             const uint32_t fin = kColS + 128 * (nchunks & 1);
 #pragma unroll 1
@@ -875,7 +914,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
             const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
             const float *init = (w == 0) ? (a.init_state ? a.init_state + sbase : nullptr) : window_slot(a, chain, w, 0);
             float *fin = (w == sp.wins_seq - 1 && a.final_state) ? a.final_state + sbase : nullptr;
-            state_loop(a, smem, B, tmem, h, bos, eos, nchunks, init, fin);
+            const int chunk_base = (a.win_chunks > 0) ? a.win_chunks * w : 0;
+            state_loop(a, smem, B, tmem, n, h, bos, eos, nchunks, chunk_base, init, fin);
         }
         if (B->abort != 0 && warp == kFirstStateWarp && (threadIdx.x & 31) == 0) {
             // drain any MMA still in flight before the tensor memory is released

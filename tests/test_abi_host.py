@@ -92,9 +92,21 @@ def test_prefill_rejects_bad_arguments_on_host(lib, over, expect):
 
 
 def test_prefill_ex_rejects_misaligned_workspace_on_host(lib):
-    r = lib.kda_prefill_ex(A16, A16, A16, A16, A16, A16, None, A16, None, 1, 32, 2, 0.1, -5.0, 0, A16 + 8, 1 << 20,
-                           None)
+    r = lib.kda_prefill_ex(A16, A16, A16, A16, A16, A16, None, A16, None, 1, 32, 2, 0.1, -5.0, 0, None, None, 0, 0,
+                           A16 + 8, 1 << 20, None)
     assert r == K.KDA_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("every,ck,offs,rows,expect", [(48, A16, A16, 4, K.KDA_ERR_INVALID_ARG),
+                                                        (-32, A16, A16, 4, K.KDA_ERR_INVALID_ARG),
+                                                        (64, None, A16, 4, K.KDA_ERR_INVALID_ARG),
+                                                        (64, A16, None, 4, K.KDA_ERR_INVALID_ARG),
+                                                        (64, A16, A16, 0, K.KDA_ERR_INVALID_ARG),
+                                                        (64, A16 + 4, A16, 4, K.KDA_ERR_MISALIGNED)])
+def test_prefill_ex_checkpoint_arguments_on_host(lib, every, ck, offs, rows, expect):
+    r = lib.kda_prefill_ex(A16, A16, A16, A16, A16, A16, None, A16, None, 1, 32, 2, 0.1, -5.0, 0, ck, offs, rows, every,
+                           None, 0, None)
+    assert r == expect
 
 
 @pytest.mark.parametrize("over,expect", [
