@@ -314,10 +314,12 @@ def run_ours(args):
                     "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": round(p_tflops / peaks["bf16_tflops"], 5),
                                "flop_per_launch": prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD}}
+    d_kernel = decode_kernel_name(args.decode_rows * dcfg.num_heads, sms)
     decode_roof = {"bound": "hbm", "achieved": round(d_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                    "frac": round(d_gbs / peaks["hbm_gbs"], 5),
-                   "traffic": scaled_traffic(traffic, "kda_decode_kernel", args.decode_rows * dcfg.num_heads),
-                   "kernel": "kda_decode_kernel", "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes}
+                   "traffic": scaled_traffic(traffic, f"{d_kernel}<{args.state_dtype}>",
+                                             args.decode_rows * dcfg.num_heads),
+                   "kernel": d_kernel, "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes}
     dominant = prefill_roof if p_mean >= d_mean else decode_roof
     line = {
         "metric": METRIC, "value": round(p_rate, 1), "unit": "tokens*heads/s", "n_gpus": world,
@@ -411,6 +413,12 @@ def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws):
             "prefill_ms": round(p_ms, 4), "decode_ms": round(d_ms, 4),
             "decode_value": round(args.decode_rows * dcfg.num_heads * world / (d_ms * 1e-3), 1),
             "decode_unit": "rows*heads/s"}
+
+
+def decode_kernel_name(items: int, sms: int) -> str:
+    """The decode kernel the library launches for one token per row: the streaming
+    schedule from 4 (row, head) items per SM on, the register schedule below that."""
+    return "kda_decode_stream_kernel" if items >= 4 * sms else "kda_decode_kernel"
 
 
 def source_digest(kernel_file: str) -> str:

@@ -951,26 +951,35 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
         const int i = idx / kCarryCols, cc = idx % kCarryCols;
         S[i][cc] = a.init_state ? a.init_state[sbase + (size_t)i * kHeadDim + c0 + cc] : 0.0f;
     }
-    __syncthreads();
     const int i = tid >> 1;          // output row
     const int cq = (tid & 1) * 4;    // four of the block's columns
+    // Row i of every window map is read by this thread only; all 32 vectors of a row are
+    // requested at once, and the next window's row as soon as this window's FMAs are done.
+    float4 m4[kHeadDim / 4];
+    auto load_row = [&](int w) {
+        const float4 *M = reinterpret_cast<const float4 *>(window_slot(a, chain, w, 2) + (size_t)i * kHeadDim);
+#pragma unroll
+        for (int j = 0; j < kHeadDim / 4; ++j) m4[j] = __ldcg(M + j);
+    };
+    load_row(0);
+    __syncthreads();
     for (int w = 0; w + 1 < sp.wins_seq; ++w) {
-        const float *M = window_slot(a, chain, w, 2) + (size_t)i * kHeadDim;
-        const float *E = window_slot(a, chain, w, 1) + (size_t)i * kHeadDim + c0 + cq;
-        float acc[4] = {E[0], E[1], E[2], E[3]};
-#pragma unroll 4
-        for (int j = 0; j < kHeadDim; j += 4) {
-            const float4 m4 = *reinterpret_cast<const float4 *>(M + j);
-            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+        const float4 e4 = __ldcg(reinterpret_cast<const float4 *>(window_slot(a, chain, w, 1) + (size_t)i * kHeadDim +
+                                                                  c0 + cq));
+        float acc[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+        for (int j = 0; j < kHeadDim / 4; ++j) {
+            const float mv[4] = {m4[j].x, m4[j].y, m4[j].z, m4[j].w};
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                const float4 s4 = *reinterpret_cast<const float4 *>(&S[j + jj][cq]);
+                const float4 s4 = *reinterpret_cast<const float4 *>(&S[4 * j + jj][cq]);
                 acc[0] = fmaf(mv[jj], s4.x, acc[0]);
                 acc[1] = fmaf(mv[jj], s4.y, acc[1]);
                 acc[2] = fmaf(mv[jj], s4.z, acc[2]);
                 acc[3] = fmaf(mv[jj], s4.w, acc[3]);
             }
         }
+        if (w + 2 < sp.wins_seq) load_row(w + 1);
         __syncthreads();
         *reinterpret_cast<float4 *>(&S[i][cq]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         *reinterpret_cast<float4 *>(window_slot(a, chain, w + 1, 0) + (size_t)i * kHeadDim + c0 + cq) =
