@@ -1,28 +1,32 @@
 // Chunk-32 varlen KDA prefill, tcgen05 / TMEM version (sm_103a).
 //
-// Same chunk algebra as "FlashInfer PR #4262: CAKE KDA Prefill Highlights", section 2, in
-// the reassociated form (Wk = T'Kbar, Wv = T'V, Q' = Qbar - Mqk Wk, Ov = Mqk Wv):
-//     U = Wv - Wk S,   O = Ov + Q' S,   S_new = Diag(2^G_last) S + Kr^T U.
-//
-// As on the page, the FP32 recurrent state stays in tensor memory for the whole sequence
-// and the state-sized products run on tcgen05; unlike the page, the accumulator is
-// preloaded so that the projection itself produces U and O:
-//     D1^T[dv, 0:32]  = Wv^T,   D1^T[dv, 32:64] = Ov^T         (producer tcgen05.st)
-//     D1^T += S^T [-Wk; Q']^T      M128 N64 K128, kind::tf32, A = S^T read from TMEM
-//     S_nxt = S_cur Diag(2^G_last)                              (state warps, TMEM -> TMEM)
-//     S_nxt^T += U^T Kr            M128 N128 K32, kind::tf32, A = U^T read from TMEM
-// so nothing on the serial chain passes through registers except the decay. The state
-// is ping-ponged between two TMEM buffers so that the decay runs while the projection
-// reads the previous buffer.
+// Chunk algebra of "FlashInfer PR #4262: CAKE KDA Prefill Highlights", section 2. With
+// T' = (I + Diag(beta) A)^-1 Diag(beta) the chunk's WY factor and Kbar, Qbar, Kr the decayed
+// keys and queries, the page's U = T'(V - Kbar S) and O = Mqk U + Qbar S are reassociated
+// around the residual R = V - Kbar S:
+//     S_new = Diag(2^G_last) S + Kt^T R,   Kt = T'^T Kr   (32 x 128)
+//     O     = Qbar S + Bo R,               Bo = Mqk T'    (32 x 32)
+// so U, Wk = T' Kbar and Wv = T' V are never formed. As on the page, the FP32 recurrent
+// state stays in tensor memory for the whole sequence and the state-sized products run on
+// tcgen05; the accumulator is preloaded so that the projection itself produces R:
+//     D1^T[dv, 0:32]  = V^T,  D1^T[dv, 32:64] = 0                  (producer tcgen05.st)
+//     D1^T += S^T [-Kbar; Qbar]^T   M128 N64 K128, kind::tf32, A = S^T read from TMEM
+//                                   -> D1^T = [R^T | (Qbar S)^T]
+//     D1^T[:, 32:64] += R^T Bo^T    M128 N32 K32,  A = R^T read from TMEM      -> O^T
+//     S_nxt = S_cur Diag(2^G_last)                                  (state warps, TMEM -> TMEM)
+//     S_nxt^T += R^T Kt             M128 N128 K32, A = R^T read from TMEM
+// Kt^T = Kr^T T' is one more small tcgen05 product (M128 N32 K32, both operands in shared
+// memory, T' split into two TF32 terms so the product keeps FP32 accuracy), issued by the
+// producers off the serial chain. The state is ping-ponged between two TMEM buffers so that
+// the decay runs while the projection reads the previous buffer.
 //
 // Warp roles (one CTA per (sequence, head) chain, 12 warps):
 //   warps 0-7  producers: raw loads (cp.async), gate and decay products, pair products
-//              (mma.sync), [Wk | Wv] by an FP32 forward substitution through the unit lower
-//              triangular (I + Diag(beta) A) -- the 32 x 32 inverse of the page is never formed
-//              --, Q'/Ov (mma.sync), then the chunk operands into a two-deep SMEM stage ring
-//              and Wv/Ov into TMEM;
+//              Mqk and Diag(beta) A (mma.sync), (I + Diag(beta) A)^-1 in FP32 by 16 x 16 blocks
+//              (forward substitution on the diagonal blocks, one product pair for the
+//              off-diagonal block), Bo (mma.sync, TF32), Kt (tcgen05), V^T into TMEM;
 //   warps 8-11 state warps (one per TMEM lane quadrant): initial/final state, the decay,
-//              the output read-out and store; lane 0 of warp 8 issues the MMAs.
+//              the output read-out and store; lane 0 of warp 8 issues the state MMAs.
 // Exponent range: per 16-token half, factors are anchored at the half's 8th token, built
 // as running products of the per-token decays and their inverses (no per-element exp of a
 // prefix); the off-diagonal block factors through the half boundary (both factors <= 1).
@@ -47,7 +51,6 @@ constexpr int kBarProd = 1;   // named barrier of the producer warps
 constexpr int kBarState = 2;  // named barrier of the state warps
 
 constexpr int kRowB = 136;  // padded bf16 row stride (ldmatrix operands)
-constexpr int kRowF = 132;  // padded fp32 row stride
 constexpr int kSq = 36;     // fp32 32 x 32 tiles
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -58,45 +61,53 @@ constexpr int kRawA = kRawK + 8192;
 constexpr int kRawV = kRawA + 8192;               // bf16 [32][136]
 constexpr int kRawBeta = kRawV + 32 * kRowB * 2;  // fp32 [32]
 constexpr int kStage0 = kRawBeta + 128;
-constexpr int kStW = 0;                           // tf32, K-major core matrices, [64 tok][128 dk]
-constexpr int kStKr = 32768;                      // tf32, K-major core matrices, [128 dk][32 tok]
-constexpr int kStDec = 49152;                     // fp32 [128]
+// One stage per chunk in flight: the operands the state MMAs read.
+constexpr int kWLbo = 144;                        // [-Kbar; Qbar]: core matrices adjacent along K are
+constexpr int kWSbo = 32 * kWLbo;                 //   144 B apart, so a warp's row stores hit all banks
+constexpr int kStW = 0;                           // tf32 [64 tok][128 dk], K-major core matrices
+constexpr int kStKt = kStW + 8 * kWSbo;           // tf32 [128 dk][32 tok]: Kr, then Kt in place
+constexpr int kStBo = kStKt + 16384;              // tf32 [32 tok][32 tok]: Bo = Mqk T'
+constexpr int kStDec = kStBo + 4096;              // fp32 [128]: 2^G_last
 constexpr int kStageBytes = kStDec + 512;
 constexpr int kPair = kStage0 + 2 * kStageBytes;  // 3 x [48][136] bf16
 constexpr int kPairQ = kPair;
 constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
 constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
 constexpr int kPairEnd = kPairKR + 48 * kRowB * 2;
-constexpr int kWvS = kPair;                       // fp32 [32][132], aliases the dead pair operands
-constexpr int kOvS = kWvS + 32 * kRowF * 4;       // fp32 [32][132]; holds Wk before it holds Ov
-constexpr int kWkS = kOvS;
-constexpr int kKbar = kPairEnd;                   // bf16 [32][136]
-constexpr int kQbar = kKbar + 32 * kRowB * 2;     // bf16 [32][136]
-constexpr int kWkB = kQbar + 32 * kRowB * 2;      // bf16 [32][136]
-constexpr int kNt = kWkB + 32 * kRowB * 2;        // fp32 [32][36]: (Diag(beta) A)^T
+constexpr int kAtHi = kPairEnd;                   // tf32 [32][32] core matrices: T'^T, high part
+constexpr int kAtLo = kAtHi + 4096;               // tf32: T'^T minus the high part (read by the Kt
+                                                  //   MMA while the next chunk's pair operands form)
+constexpr int kTinv = kAtLo + 4096;               // fp32 [32][36]: (I + Diag(beta) A)^-1 (its diagonal
+constexpr int kPscr = kTinv + 32 * kSq * 4;       //   blocks form while Mqk still reads the pair operands);
+                                                  // fp32 [16][16]: N21 T11 (and 2 x [8][8] before)
+constexpr int kNt = kPscr + 1024;                 // fp32 [32][36]: (Diag(beta) A)^T
 constexpr int kMq = kNt + 32 * kSq * 4;           // fp32 [32][36]: Mqk
 constexpr int kQuart = kMq + 32 * kSq * 4;        // fp32 [4][128]: per-quarter decay products
-constexpr int kOst = kQuart + 4 * 128 * 4;        // bf16 [32][136]: output staging
+constexpr int kBetaS = kQuart + 4 * 128 * 4;      // fp32 [32]: beta of the chunk (raw copy is refilled early)
+constexpr int kOst = kBetaS + 128;                // bf16 [32][136]: output staging
 constexpr int kBars = kOst + 32 * kRowB * 2;
 constexpr int kSmemTc = kBars + 128;
-static_assert(kOvS + 32 * kRowF * 4 <= kPairEnd, "Wv/Ov staging fits in the pair region");
-static_assert(kStage0 % 128 == 0 && kStageBytes % 128 == 0, "stage alignment");
+static_assert(kStage0 % 128 == 0 && kStageBytes % 128 == 0 && kAtHi % 128 == 0, "operand alignment");
 static_assert(kSmemTc <= 227 * 1024, "one CTA per SM");
 
 // ---- tensor-memory map (columns; 512 allocated)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;     // S^T ping-pong: [0,128) and [128,256)
 constexpr uint32_t kColD1 = 256;  // D1 double buffer: [256,320) and [320,384)
+constexpr uint32_t kColKt = 384;  // Kt^T (lane = dk, column = token), producer-owned
 
 constexpr uint32_t kIdescG1 = instr_desc(2, 128, 64);   // tf32, M128 N64
 constexpr uint32_t kIdescG2 = instr_desc(2, 128, 128);  // tf32, M128 N128
+constexpr uint32_t kIdescN32 = instr_desc(2, 128, 32);  // tf32, M128 N32
 
 struct Bars {
     uint64_t prep[2];    // producers -> state warps: stage s filled (count kProdThreads)
     uint64_t g1;         // projection MMA complete (tcgen05.commit)
+    uint64_t go;         // output MMA complete (tcgen05.commit)
     uint64_t g2;         // state update MMA complete (tcgen05.commit)
     uint64_t g2s[2];     // state update of a chunk on stage s complete (tcgen05.commit)
     uint64_t oread[2];   // D1 buffer b read out by the state warps (count kStateThreads)
+    uint64_t kt;         // producers' Kt MMA complete (tcgen05.commit)
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -142,6 +153,13 @@ __device__ __forceinline__ void st_bf16(uint8_t *base, int elem, float x) {
 __device__ __forceinline__ int core_off_tf32(int row, int col, int sbo) {
     return (row >> 3) * sbo + (col >> 2) * 128 + (row & 7) * 16 + (col & 3) * 4;
 }
+
+// Byte offset of element (token, dk) of the [-Kbar; Qbar] operand (K-major, padded K stride).
+__device__ __forceinline__ int w_off(int row, int col) {
+    return (row >> 3) * kWSbo + (col >> 2) * kWLbo + (row & 7) * 16 + (col & 3) * 4;
+}
+
+__device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -215,6 +233,95 @@ __device__ __forceinline__ void load_vb(const PrefillArgs &a, uint8_t *smem, int
 
 // ------------------------------------------------------------------ producers
 
+// Kt^T (TMEM lane = dk, column = token) -> the stage's Kt operand (tf32, [dk][token]).
+// Producer warps w and w + 4 share lane quadrant w % 4 and take 16 token columns each.
+__device__ __forceinline__ void kt_to_stage(uint32_t tmem, uint8_t *stage, int warp, int lane) {
+    const int quad = warp & 3, half = warp >> 2;
+    const int dk = 32 * quad + lane;
+    float v[16];
+    tmem_ld16(tmem + ((uint32_t)(32 * quad) << 16) + kColKt + 16 * half, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e4 = 0; e4 < 4; ++e4)
+        *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(dk, 16 * half + 4 * e4, 1024)) =
+            make_float4(tf32f(v[4 * e4]), tf32f(v[4 * e4 + 1]), tf32f(v[4 * e4 + 2]), tf32f(v[4 * e4 + 3]));
+}
+
+// V^T of the chunk into its D1 buffer (lane = dv, column = token); the output pass also
+// zeroes the 32 columns the projection accumulates Qbar S into.
+template <bool kPass1>
+__device__ __forceinline__ void v_to_tmem(uint32_t tmem, const uint8_t *rv, int db, int warp, int lane) {
+    if (kPass1 && warp >= 4) return;
+    const int quad = warp & 3;
+    float v0[16], v1[16];
+    if (warp < 4) {
+        const int dv = 32 * quad + lane;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            v0[t] = bfv(rv, t * kRowB + dv);
+            v1[t] = bfv(rv, (16 + t) * kRowB + dv);
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) v0[t] = v1[t] = 0.0f;
+    }
+    // output pass: D1 = [V | 0] (64 columns per buffer); window pass: D1 = V (32)
+    const uint32_t col = kPass1 ? kColD1 + 32 * db : kColD1 + 64 * db + 32 * (warp >> 2);
+    const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + col;
+    tmem_st16(taddr, v0);
+    tmem_st16(taddr + 16, v1);
+    tmem_wait_st();
+}
+
+// (I + N_d)^-1 of the 16 x 16 diagonal block at (o, o) of a strictly lower triangular N
+// (given transposed: nt[j * kSq + i] = N[i][j]) into inv[(o + i) * kSq + o + j], by one warp:
+// the two 8 x 8 diagonal blocks by forward substitution (lanes 0-15, one column each; lanes
+// 16-31 zero the upper 8 x 8 block), then the lower block -T22 N21 T11. `scr`: 64 floats.
+__device__ __forceinline__ void invert_diag16(const float *nt, float *inv, float *scr, int o, int lane) {
+    if (lane < 16) {
+        const int b = o + 8 * (lane >> 3), cc = lane & 7;
+        float t[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) t[m] = (m == cc) ? 1.0f : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 7; ++j) {
+            const float tj = t[j];
+            const float4 n0 = *reinterpret_cast<const float4 *>(nt + (b + j) * kSq + b);
+            const float4 n1 = *reinterpret_cast<const float4 *>(nt + (b + j) * kSq + b + 4);
+            const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+            for (int m = j + 1; m < 8; ++m) t[m] = fmaf(-nv[m], tj, t[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) inv[(b + m) * kSq + b + cc] = t[m];
+    } else {
+        const int r = (lane - 16) >> 1, c4 = 4 * (lane & 1);
+        *reinterpret_cast<float4 *>(inv + (o + r) * kSq + o + 8 + c4) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    __syncwarp();
+    const int i = lane >> 2, j2 = 2 * (lane & 3);
+    const int r0 = o + 8;
+    float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+    for (int l = 0; l < 8; ++l) {
+        const float nv = nt[(o + l) * kSq + r0 + i];
+        const float2 tv = *reinterpret_cast<const float2 *>(inv + (o + l) * kSq + o + j2);
+        p0 = fmaf(nv, tv.x, p0);
+        p1 = fmaf(nv, tv.y, p1);
+    }
+    *reinterpret_cast<float2 *>(scr + i * 8 + j2) = make_float2(p0, p1);
+    __syncwarp();
+    float q0 = 0.0f, q1 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float tv = inv[(r0 + i) * kSq + r0 + k];
+        const float2 pv = *reinterpret_cast<const float2 *>(scr + k * 8 + j2);
+        q0 = fmaf(tv, pv.x, q0);
+        q1 = fmaf(tv, pv.y, q1);
+    }
+    *reinterpret_cast<float2 *>(inv + (r0 + i) * kSq + o + j2) = make_float2(-q0, -q1);
+}
+
 template <bool kPass1>
 __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int n, int h, int bos,
                               int eos, int nchunks) {
@@ -224,12 +331,10 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     uint8_t *const pairQ = smem + kPairQ;
     uint8_t *const pairKL = smem + kPairKL;
     uint8_t *const pairKR = smem + kPairKR;
-    uint8_t *const kbar_s = smem + kKbar;
-    uint8_t *const qbar_s = smem + kQbar;
-    uint8_t *const wkb_s = smem + kWkB;
-    float *const wv_s = reinterpret_cast<float *>(smem + kWvS);
-    float *const ov_s = reinterpret_cast<float *>(smem + kOvS);
-    float *const wk_s = reinterpret_cast<float *>(smem + kWkS);
+    float *const tinv = reinterpret_cast<float *>(smem + kTinv);
+    float *const pscr = reinterpret_cast<float *>(smem + kPscr);
+    uint8_t *const at_hi = smem + kAtHi;
+    uint8_t *const at_lo = smem + kAtLo;
     float *const nt_s = reinterpret_cast<float *>(smem + kNt);
     float *const mq_s = reinterpret_cast<float *>(smem + kMq);
     float *const quart_s = reinterpret_cast<float *>(smem + kQuart);
@@ -238,6 +343,9 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     const uint8_t *const ra = smem + kRawA;
     const uint8_t *const rv = smem + kRawV;
     const float *const rb = reinterpret_cast<const float *>(smem + kRawBeta);
+    float *const beta_s = reinterpret_cast<float *>(smem + kBetaS);
+    bool aborted = false;
+    int kt_parity = -1;  // thread 0: phase of an issued Kt MMA not yet observed complete
 
     if (nchunks > 0) {
         const int L0 = min(kChunk, eos - bos);
@@ -249,11 +357,16 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = bos + kChunk * c;
         const int L = min(kChunk, eos - t0);
-        const int ps = c & 1;
+        const int ps = c & 1, db = c & 1;
         uint8_t *const stage = smem + kStage0 + ps * kStageBytes;
         cp_async_wait<0>();
-        bar_named(kBarProd, kProdThreads);
-        if (c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status)) break;
+        {  // stage ps is free once the state update of chunk c - 2 has read it
+            const bool lost = c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status);
+            if (bar_any(kBarProd, kProdThreads, lost)) {
+                aborted = true;
+                break;
+            }
+        }
 
         // ---- 1. decays, anchored factors, chunk operands. Thread = (channel pair, 8-token
         //      quarter). With d the per-token decay, every factor is a running product of d or
@@ -359,17 +472,19 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
                 }
                 const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
-                st_pair(kbar_s, i * kRowB + ch, k0 * fb0, k1 * fb1);
-                if (!kPass1) st_pair(qbar_s, i * kRowB + ch, q0 * fb0, q1 * fb1);
+                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) = make_float2(tf32f(-k0 * fb0), tf32f(-k1 * fb1));
+                if (!kPass1)
+                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) =
+                        make_float2(tf32f(q0 * fb0), tf32f(q1 * fb1));
                 kr0[ii] = __uint_as_float(to_tf32(k0 * (S0[ii] * post0)));  // 2^(G_L - G_i)
                 kr1[ii] = __uint_as_float(to_tf32(k1 * (S1[ii] * post1)));
             }
 #pragma unroll
             for (int h4 = 0; h4 < 2; ++h4) {
                 const int i0 = 8 * qt + 4 * h4;
-                *reinterpret_cast<float4 *>(stage + kStKr + core_off_tf32(ch, i0, 1024)) =
+                *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch, i0, 1024)) =
                     make_float4(kr0[4 * h4], kr0[4 * h4 + 1], kr0[4 * h4 + 2], kr0[4 * h4 + 3]);
-                *reinterpret_cast<float4 *>(stage + kStKr + core_off_tf32(ch + 1, i0, 1024)) =
+                *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch + 1, i0, 1024)) =
                     make_float4(kr1[4 * h4], kr1[4 * h4 + 1], kr1[4 * h4 + 2], kr1[4 * h4 + 3]);
             }
             if (!ok) report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
@@ -377,14 +492,39 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 *reinterpret_cast<float2 *>(stage + kStDec + 4 * ch) =
                     make_float2(T[0].x * T[1].x * T[2].x * T[3].x, T[0].y * T[1].y * T[2].y * T[3].y);
         }
+        // ---- 1b. Hand-off of chunk c - 1 (its Kt MMA ran during phase 1): Kt into its stage in
+        //      place of Kr, then the stage is released to the state warps. V^T of chunk c into
+        //      its D1 buffer and beta aside, so the raw buffers can refill with chunk c + 1.
+        {
+            bool lost = c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status);
+            if (c >= 1 && ptid == 0) {
+                lost = lost || !wait_or_abort(&B->kt, (c - 1) & 1, B, a.status);
+                kt_parity = -1;
+            }
+            if (bar_any(kBarProd, kProdThreads, lost)) {
+                aborted = true;
+                break;
+            }
+        }
+        tc_fence_after();
+        if (c >= 1) kt_to_stage(tmem, smem + kStage0 + (ps ^ 1) * kStageBytes, warp, lane);
+        v_to_tmem<kPass1>(tmem, rv, db, warp, lane);
+        if (ptid < kChunk) beta_s[ptid] = rb[ptid];
+        if (c >= 1) {
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&B->prep[ps ^ 1]);
+        }
         bar_named(kBarProd, kProdThreads);
         if (c + 1 < nchunks) {
             const int t1 = t0 + kChunk;
             load_qka(a, smem, t1, min(kChunk, eos - t1), h, ptid);
+            load_vb(a, smem, t1, min(kChunk, eos - t1), h, ptid);
         }
         cp_async_commit();
 
-        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5)
+        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5).
+        //      The warps holding a diagonal block of N invert I + N there at once.
         if (warp < 6) {
           if (!(kPass1 && warp < 3)) {  // the Mqk blocks are not needed by the window pass
             const int which = warp / 3;
@@ -413,163 +553,112 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     if (which == 0) {
                         mq_s[i * kSq + j] = (j <= i) ? val : 0.0f;
                     } else {
-                        nt_s[j * kSq + i] = (j < i) ? val * rb[i] : 0.0f;
+                        nt_s[j * kSq + i] = (j < i) ? val * beta_s[i] : 0.0f;
                     }
                 }
+            }
+            if (which == 1 && blk < 2) {
+                __syncwarp();
+                invert_diag16(nt_s, tinv, pscr + 64 * blk, 16 * blk, lane);
             }
           }
         } else {
             for (int idx = ptid - 192; idx < 256; idx += 64) {
                 const int i = idx >> 4, j = 16 + (idx & 15);
                 mq_s[i * kSq + j] = 0.0f;
-                nt_s[j * kSq + i] = 0.0f;
+                tinv[i * kSq + j] = 0.0f;  // upper-right block of the inverse
             }
         }
         bar_named(kBarProd, kProdThreads);
 
-        // ---- 3. (I + Diag(beta) A) [Wk | Wv] = Diag(beta) [Kbar | V] by forward substitution in
-        //      FP32, one column per thread (warps 0-3: Kbar columns, warps 4-7: V columns).
+        // ---- 3. off-diagonal block of the inverse: T21 = -T22 N21 T11
         {
-            const int cc = ptid & 127;
-            const uint8_t *X = (ptid < 128) ? kbar_s : rv;
-            float acc[32];
+            const int i = ptid >> 4, j = ptid & 15;
+            float p = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = rb[i] * bfv(X, i * kRowB + cc);
-#pragma unroll
-            for (int j = 0; j < 31; ++j) {
-                const float wj = acc[j];
-#pragma unroll
-                for (int m = (j + 1) >> 2; m < 8; ++m) {
-                    const float4 n4 = *reinterpret_cast<const float4 *>(nt_s + j * kSq + 4 * m);
-                    if (4 * m + 0 > j) acc[4 * m + 0] = fmaf(-n4.x, wj, acc[4 * m + 0]);
-                    if (4 * m + 1 > j) acc[4 * m + 1] = fmaf(-n4.y, wj, acc[4 * m + 1]);
-                    if (4 * m + 2 > j) acc[4 * m + 2] = fmaf(-n4.z, wj, acc[4 * m + 2]);
-                    if (4 * m + 3 > j) acc[4 * m + 3] = fmaf(-n4.w, wj, acc[4 * m + 3]);
-                }
-            }
-            float *dst = (ptid < 128) ? wk_s : wv_s;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dst[i * kRowF + cc] = acc[i];
+            for (int l = 0; l < 16; ++l) p = fmaf(nt_s[l * kSq + 16 + i], tinv[l * kSq + j], p);
+            pscr[i * 16 + j] = p;
         }
         bar_named(kBarProd, kProdThreads);
-        if (c + 1 < nchunks) {
-            const int t1 = t0 + kChunk;
-            load_vb(a, smem, t1, min(kChunk, eos - t1), h, ptid);
-        }
-        cp_async_commit();
-
-        // ---- 4. -Wk into the stage's W rows 0-31 (tf32 core matrices; lanes walk the 8 rows of
-        //      a core matrix so the stores are contiguous) and a bf16 copy of Wk for step 5.
+        {
+            const int i = ptid >> 4, j = ptid & 15;
+            float p = 0.0f;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int idx = ptid + kProdThreads * m;  // 0 .. 1023
-            const int row = ((idx >> 8) << 3) + (idx & 7);
-            const int grp = (idx >> 3) & 31;
-            const float4 w = *reinterpret_cast<const float4 *>(wk_s + row * kRowF + 4 * grp);
-            *reinterpret_cast<float4 *>(stage + kStW + core_off_tf32(row, 4 * grp, 4096)) =
-                make_float4(__uint_as_float(to_tf32(-w.x)), __uint_as_float(to_tf32(-w.y)),
-                            __uint_as_float(to_tf32(-w.z)), __uint_as_float(to_tf32(-w.w)));
-            *reinterpret_cast<uint2 *>(wkb_s + (row * kRowB + 4 * grp) * 2) =
-                make_uint2(pack_bf16(w.x, w.y), pack_bf16(w.z, w.w));
+            for (int k = 0; k < 16; ++k) p = fmaf(tinv[(16 + i) * kSq + 16 + k], pscr[k * 16 + j], p);
+            tinv[(16 + i) * kSq + j] = -p;
         }
         bar_named(kBarProd, kProdThreads);
 
-        // ---- 5. Q' = Qbar - Mqk Wk (-> stage W rows 32-63), Ov = Mqk Wv (output pass only)
-        if (!kPass1) {
-            uint32_t am[2][2][4], amn[2][2][4];
+        // ---- 4. T' = T Diag(beta), stored as T'^T (row j, K index i) in two TF32 parts
+        {
+            const int j = ptid & 31, q = ptid >> 5;  // T'[4q .. 4q + 3][j]
+            const float bj = beta_s[j];
+            float hi[4], lo[4];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = 16 * mt + g + 8 * (r & 1);
-                        const int col = 16 * ks + 2 * t4 + 8 * (r >> 1);
-                        const float2 v2 = *reinterpret_cast<const float2 *>(mq_s + row * kSq + col);
-                        am[mt][ks][r] = pack_bf16(v2.x, v2.y);
-                        amn[mt][ks][r] = pack_bf16(-v2.x, -v2.y);
-                    }
-                }
+            for (int r = 0; r < 4; ++r) {
+                const float x = tinv[(4 * q + r) * kSq + j] * bj;
+                hi[r] = tf32f(x);
+                lo[r] = tf32f(x - hi[r]);
             }
-            float qa[2][2][4], oa[2][2][4] = {};
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                for (int nl = 0; nl < 2; ++nl) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int row = 16 * mt + g + 8 * hr;
-                        const int col = 16 * warp + 8 * nl + 2 * t4;
-                        qa[mt][nl][2 * hr] = bfv(qbar_s, row * kRowB + col);
-                        qa[mt][nl][2 * hr + 1] = bfv(qbar_s, row * kRowB + col + 1);
-                    }
-                }
-            }
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                uint32_t bw[4];
-                const int krow = 16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4_trans(bw, smem_addr(wkb_s + (krow * kRowB + 16 * warp + (lane >> 4) * 8) * 2));
-                uint32_t bv[2][2];
-#pragma unroll
-                for (int nl = 0; nl < 2; ++nl) {
-                    const int col = 16 * warp + 8 * nl + g;
-                    const int k0 = 16 * ks + 2 * t4;
-                    bv[nl][0] = pack_bf16(wv_s[k0 * kRowF + col], wv_s[(k0 + 1) * kRowF + col]);
-                    bv[nl][1] = pack_bf16(wv_s[(k0 + 8) * kRowF + col], wv_s[(k0 + 9) * kRowF + col]);
-                }
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                    for (int nl = 0; nl < 2; ++nl) {
-                        mma_bf16_16816(qa[mt][nl], amn[mt][ks], bw[2 * nl], bw[2 * nl + 1]);
-                        mma_bf16_16816(oa[mt][nl], am[mt][ks], bv[nl][0], bv[nl][1]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                for (int nl = 0; nl < 2; ++nl) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int row = 16 * mt + g + 8 * hr;
-                        const int col = 16 * warp + 8 * nl + 2 * t4;
-                        *reinterpret_cast<float2 *>(stage + kStW + core_off_tf32(32 + row, col, 4096)) =
-                            make_float2(__uint_as_float(to_tf32(qa[mt][nl][2 * hr])),
-                                        __uint_as_float(to_tf32(qa[mt][nl][2 * hr + 1])));
-                        *reinterpret_cast<float2 *>(ov_s + row * kRowF + col) =
-                            make_float2(oa[mt][nl][2 * hr], oa[mt][nl][2 * hr + 1]);
-                    }
-                }
-            }
-        }
-        bar_named(kBarProd, kProdThreads);
-
-        // ---- 6. Wv^T / Ov^T into the chunk's D1 buffer (needs its previous use read out)
-        const int db = c & 1;
-        if (c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status)) break;
-        tc_fence_after();
-        if (!kPass1 || warp < 4) {
-            const float *src = (warp < 4) ? wv_s : ov_s;
-            const int quad = warp & 3;
-            const int dv = 32 * quad + lane;
-            float v0[16], v1[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                v0[t] = src[t * kRowF + dv];
-                v1[t] = src[(16 + t) * kRowF + dv];
-            }
-            // output pass: D1 = [Wv | Ov] (64 columns per buffer); window pass: D1 = Wv (32)
-            const uint32_t col = kPass1 ? kColD1 + 32 * db : kColD1 + 64 * db + 32 * (warp >> 2);
-            const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + col;
-            tmem_st16(taddr, v0);
-            tmem_st16(taddr + 16, v1);
-            tmem_wait_st();
+            const int off = core_off_tf32(j, 4 * q, 1024);
+            *reinterpret_cast<float4 *>(at_hi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<float4 *>(at_lo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
         }
         fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(&B->prep[ps]);
+        bar_named(kBarProd, kProdThreads);
+
+        // ---- 5. Kt^T = Kr^T T' on tcgen05 (M128 N32 K32, both operands in shared memory; read
+        //      back at the next hand-off), and Bo = Mqk T' (output pass) by mma.sync TF32.
+        if (ptid == 0) {
+            tc_fence_after();
+            const uint32_t kra = smem_addr(stage + kStKt), ah = smem_addr(at_hi), al = smem_addr(at_lo);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_tf32_ss(tmem + kColKt, smem_desc_kmajor(kra + 256 * s, 128, 1024),
+                            smem_desc_kmajor(ah + 256 * s, 128, 1024), kIdescN32, s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_tf32_ss(tmem + kColKt, smem_desc_kmajor(kra + 256 * s, 128, 1024),
+                            smem_desc_kmajor(al + 256 * s, 128, 1024), kIdescN32, true);
+            mma_commit(&B->kt);
+            kt_parity = c & 1;
+        }
+        __syncwarp();
+        if (!kPass1) {
+            // warp = one 16 x 8 tile of Bo; Bo is lower triangular, so K steps outside
+            // [column tile, row tile] contribute nothing
+            const int mt = warp >> 2, nt = warp & 3;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                if (ks < nt || ks > 2 * mt + 1) continue;
+                const int r0 = 16 * mt + g, k0 = 8 * ks + t4;
+                const uint32_t af[4] = {to_tf32(mq_s[r0 * kSq + k0]), to_tf32(mq_s[(r0 + 8) * kSq + k0]),
+                                        to_tf32(mq_s[r0 * kSq + k0 + 4]), to_tf32(mq_s[(r0 + 8) * kSq + k0 + 4])};
+                const int jn = 8 * nt + g;
+                const float bj = beta_s[jn];
+                mma_tf32_1688(acc, af, to_tf32(tinv[k0 * kSq + jn] * bj), to_tf32(tinv[(k0 + 4) * kSq + jn] * bj));
+            }
+            const int i0 = 16 * mt + g, j0 = 8 * nt + 2 * t4;
+            *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0, j0, 1024)) =
+                make_float2(tf32f(acc[0]), tf32f(acc[1]));
+            *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0 + 8, j0, 1024)) =
+                make_float2(tf32f(acc[2]), tf32f(acc[3]));
+        }
+    }
+    // an aborted loop may leave this thread's last Kt MMA unobserved: drain it (bounded)
+    if (aborted && ptid == 0 && kt_parity >= 0) mbar_wait(&B->kt, (uint32_t)kt_parity);
+    // hand-off of the last chunk
+    if (!aborted && nchunks > 0) {
+        const int c = nchunks - 1;
+        const bool lost = ptid == 0 && !wait_or_abort(&B->kt, c & 1, B, a.status);
+        if (!bar_any(kBarProd, kProdThreads, lost)) {
+            tc_fence_after();
+            kt_to_stage(tmem, smem + kStage0 + (c & 1) * kStageBytes, warp, lane);
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&B->prep[c & 1]);
+        }
     }
     cp_async_wait<0>();
 }
@@ -638,8 +727,8 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
             const uint32_t wbase = smem_addr(stage + kStW);
 #pragma unroll
             for (int s = 0; s < 16; ++s)
-                mma_tf32_ts(tmem + kColD1 + 64 * db, tmem + cur + 8 * s, smem_desc_kmajor(wbase + 256 * s, 128, 4096),
-                            kIdescG1, true);
+                mma_tf32_ts(tmem + kColD1 + 64 * db, tmem + cur + 8 * s,
+                            smem_desc_kmajor(wbase + 2 * kWLbo * s, kWLbo, kWSbo), kIdescG1, true);
             mma_commit(&B->g1);
         }
         __syncwarp();
@@ -669,7 +758,14 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         if (mma_thread) {
             if (wait_or_abort(&B->g1, c & 1, B, a.status)) {
                 tc_fence_after();
-                const uint32_t kbase = smem_addr(stage + kStKr);
+                // O^T = (Qbar S)^T + R^T Bo^T, then S_nxt^T += R^T Kt (A = R^T = D1^T[:, 0:32])
+                const uint32_t obase = smem_addr(stage + kStBo);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_tf32_ts(tmem + kColD1 + 64 * db + 32, tmem + kColD1 + 64 * db + 8 * s,
+                                smem_desc_kmajor(obase + 256 * s, 128, 1024), kIdescN32, true);
+                mma_commit(&B->go);
+                const uint32_t kbase = smem_addr(stage + kStKt);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_tf32_ts(tmem + nxt, tmem + kColD1 + 64 * db + 8 * s,
@@ -680,7 +776,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         }
         __syncwarp();
         // output read-out: O^T = D1^T[:, 32:64]
-        if (!wait_or_abort(&B->g1, c & 1, B, a.status)) break;
+        if (!wait_or_abort(&B->go, c & 1, B, a.status)) break;
         tc_fence_after();
         float o0[16], o1[16];
         tmem_ld16(tmem + lane_base + kColD1 + 64 * db + 32, o0);
@@ -742,8 +838,6 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
 // after the projection has read the state.
 constexpr uint32_t kColM = 128;
 constexpr uint32_t kColD1M = 320;
-constexpr uint32_t kIdescN32 = instr_desc(2, 128, 32);  // tf32, M128 N32
-
 __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int nchunks,
                                  float *E_out, float *M_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -778,7 +872,7 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
             const uint32_t wbase = smem_addr(stage + kStW);
 #pragma unroll
             for (int s = 0; s < 16; ++s) {
-                const uint64_t bd = smem_desc_kmajor(wbase + 256 * s, 128, 4096);
+                const uint64_t bd = smem_desc_kmajor(wbase + 2 * kWLbo * s, kWLbo, kWSbo);
                 mma_tf32_ts(tmem + kColD1 + 32 * db, tmem + kColS + 8 * s, bd, kIdescN32, true);
                 mma_tf32_ts(tmem + kColD1M + 32 * db, tmem + kColM + 8 * s, bd, kIdescN32, s > 0);
             }
@@ -806,7 +900,7 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         bar_named(kBarState, kStateThreads);
         tc_fence_after();
         if (mma_thread) {
-            const uint32_t kbase = smem_addr(stage + kStKr);
+            const uint32_t kbase = smem_addr(stage + kStKt);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t bd = smem_desc_kmajor(kbase + 256 * s, 128, 1024);
@@ -888,6 +982,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         mbar_init(&B->prep[0], kProdThreads);
         mbar_init(&B->prep[1], kProdThreads);
         mbar_init(&B->g1, 1);
+        mbar_init(&B->go, 1);
+        mbar_init(&B->kt, 1);
         mbar_init(&B->g2, 1);
         mbar_init(&B->g2s[0], 1);
         mbar_init(&B->g2s[1], 1);
