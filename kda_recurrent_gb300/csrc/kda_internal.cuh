@@ -57,7 +57,8 @@ struct PrefillArgs {
     // Window schedule for short chain counts: each chain's chunks are cut into `wins`
     // windows of `win_chunks` chunks (wins = 1: one window per chain). `ws` holds, per
     // (chain, window), three FP32 128 x 128 slots: the window's start state, and the
-    // window's zero-start end state E and linear map M (S_end = M S_start + E).
+    // window's zero-start end state E and linear map M (S_end = M S_start + E), the map
+    // stored transposed (M^T, row-major).
     int32_t wins, win_chunks;
     float *ws;
     // Optional intermediate states: every `ckpt_every` tokens (a multiple of the chunk),

@@ -33,6 +33,7 @@
 // All mbarrier waits are bounded; on expiry the kernel records KDA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
 #include <algorithm>
+#include <type_traits>
 
 #include "kda_internal.cuh"
 #include "kda_mma.cuh"
@@ -49,6 +50,8 @@ constexpr int kProdThreads = kProducerWarps * 32;
 constexpr int kStateThreads = kStateWarps * 32;
 constexpr int kBarProd = 1;   // named barrier of the producer warps
 constexpr int kBarState = 2;  // named barrier of the state warps
+constexpr int kBarNpart = 3;  // 3, 4: producer warp pairs (3, 6) and (4, 7) of the diagonal N blocks
+constexpr int kKtThread = 64; // producer thread that issues and observes the Kt MMA
 
 constexpr int kRowB = 136;  // padded bf16 row stride (ldmatrix operands)
 constexpr int kSq = 36;     // fp32 32 x 32 tiles
@@ -80,7 +83,9 @@ constexpr int kAtLo = kAtHi + 4096;               // tf32: T'^T minus the high p
 constexpr int kTinv = kAtLo + 4096;               // fp32 [32][36]: (I + Diag(beta) A)^-1 (its diagonal
 constexpr int kPscr = kTinv + 32 * kSq * 4;       //   blocks form while Mqk still reads the pair operands);
                                                   // fp32 [16][16]: N21 T11 (and 2 x [8][8] before)
-constexpr int kNt = kPscr + 1024;                 // fp32 [32][36]: (Diag(beta) A)^T
+constexpr int kNpart = kPscr + 1024;              // fp32 [2][32 lanes][8]: second K half of the
+                                                  //   diagonal blocks of Diag(beta) A (mma fragments)
+constexpr int kNt = kNpart + 2048;                // fp32 [32][36]: (Diag(beta) A)^T
 constexpr int kMq = kNt + 32 * kSq * 4;           // fp32 [32][36]: Mqk
 constexpr int kQuart = kMq + 32 * kSq * 4;        // fp32 [4][128]: per-quarter decay products
 constexpr int kBetaS = kQuart + 4 * 128 * 4;      // fp32 [32]: beta of the chunk (raw copy is refilled early)
@@ -115,6 +120,10 @@ static_assert(sizeof(Bars) <= 128, "barrier block");
 
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive_named(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Named-barrier sync of `count` threads that also returns, identically to all of them,
@@ -173,19 +182,12 @@ __device__ __forceinline__ float rcp(float x) {
     return y;
 }
 
-// Per-token decay d = exp(g) of one channel and its inverse 1/d, from the raw gate a.
-__device__ __forceinline__ float gate_decay_pair(float av, int mode, float lower_bound, float &dinv) {
-    if (mode == KDA_GATE_LOWER_BOUND) {
-        const float g2 = lower_bound * kLog2e * rcp(1.0f + ex2(-av * kLog2e));  // lb sigmoid(a) log2 e
-        dinv = ex2(-g2);
-        return ex2(g2);
-    }
-    if (mode == KDA_GATE_SOFTPLUS) {
-        // exp(-softplus(a)) = 1 / (1 + e^a)
-        dinv = 1.0f + ex2(av * kLog2e);
-        return rcp(dinv);
-    }
-    dinv = ex2(-av * kLog2e);
+// Per-token decay d = exp(g) of one channel from the raw gate a.
+__device__ __forceinline__ float gate_decay(float av, int mode, float lower_bound) {
+    if (mode == KDA_GATE_LOWER_BOUND)  // exp(lb sigmoid(a))
+        return ex2(lower_bound * kLog2e * rcp(1.0f + ex2(-av * kLog2e)));
+    if (mode == KDA_GATE_SOFTPLUS)  // exp(-softplus(a)) = 1 / (1 + e^a)
+        return rcp(1.0f + ex2(av * kLog2e));
     return ex2(av * kLog2e);
 }
 
@@ -280,17 +282,22 @@ __device__ __forceinline__ void v_to_tmem(uint32_t tmem, const uint8_t *rv, int 
 __device__ __forceinline__ void invert_diag16(const float *nt, float *inv, float *scr, int o, int lane) {
     if (lane < 16) {
         const int b = o + 8 * (lane >> 3), cc = lane & 7;
+        float nv[7][8];  // nv[j][m] = N[b + m][b + j]
+#pragma unroll
+        for (int j = 0; j < 7; ++j) {
+            const float4 n0 = *reinterpret_cast<const float4 *>(nt + (b + j) * kSq + b);
+            const float4 n1 = *reinterpret_cast<const float4 *>(nt + (b + j) * kSq + b + 4);
+            nv[j][0] = n0.x, nv[j][1] = n0.y, nv[j][2] = n0.z, nv[j][3] = n0.w;
+            nv[j][4] = n1.x, nv[j][5] = n1.y, nv[j][6] = n1.z, nv[j][7] = n1.w;
+        }
         float t[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) t[m] = (m == cc) ? 1.0f : 0.0f;
 #pragma unroll
         for (int j = 0; j < 7; ++j) {
             const float tj = t[j];
-            const float4 n0 = *reinterpret_cast<const float4 *>(nt + (b + j) * kSq + b);
-            const float4 n1 = *reinterpret_cast<const float4 *>(nt + (b + j) * kSq + b + 4);
-            const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
 #pragma unroll
-            for (int m = j + 1; m < 8; ++m) t[m] = fmaf(-nv[m], tj, t[m]);
+            for (int m = j + 1; m < 8; ++m) t[m] = fmaf(-nv[j][m], tj, t[m]);
         }
 #pragma unroll
         for (int m = 0; m < 8; ++m) inv[(b + m) * kSq + b + cc] = t[m];
@@ -301,23 +308,33 @@ __device__ __forceinline__ void invert_diag16(const float *nt, float *inv, float
     __syncwarp();
     const int i = lane >> 2, j2 = 2 * (lane & 3);
     const int r0 = o + 8;
+    float nl[8];
+    float2 tl[8];
+#pragma unroll
+    for (int l = 0; l < 8; ++l) {
+        nl[l] = nt[(o + l) * kSq + r0 + i];
+        tl[l] = *reinterpret_cast<const float2 *>(inv + (o + l) * kSq + o + j2);
+    }
     float p0 = 0.0f, p1 = 0.0f;
 #pragma unroll
     for (int l = 0; l < 8; ++l) {
-        const float nv = nt[(o + l) * kSq + r0 + i];
-        const float2 tv = *reinterpret_cast<const float2 *>(inv + (o + l) * kSq + o + j2);
-        p0 = fmaf(nv, tv.x, p0);
-        p1 = fmaf(nv, tv.y, p1);
+        p0 = fmaf(nl[l], tl[l].x, p0);
+        p1 = fmaf(nl[l], tl[l].y, p1);
     }
     *reinterpret_cast<float2 *>(scr + i * 8 + j2) = make_float2(p0, p1);
     __syncwarp();
+    float tr[8];
+    float2 pl[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        tr[k] = inv[(r0 + i) * kSq + r0 + k];
+        pl[k] = *reinterpret_cast<const float2 *>(scr + k * 8 + j2);
+    }
     float q0 = 0.0f, q1 = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const float tv = inv[(r0 + i) * kSq + r0 + k];
-        const float2 pv = *reinterpret_cast<const float2 *>(scr + k * 8 + j2);
-        q0 = fmaf(tv, pv.x, q0);
-        q1 = fmaf(tv, pv.y, q1);
+        q0 = fmaf(tr[k], pl[k].x, q0);
+        q1 = fmaf(tr[k], pl[k].y, q1);
     }
     *reinterpret_cast<float2 *>(inv + (r0 + i) * kSq + o + j2) = make_float2(-q0, -q1);
 }
@@ -345,7 +362,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     const float *const rb = reinterpret_cast<const float *>(smem + kRawBeta);
     float *const beta_s = reinterpret_cast<float *>(smem + kBetaS);
     bool aborted = false;
-    int kt_parity = -1;  // thread 0: phase of an issued Kt MMA not yet observed complete
+    int kt_parity = -1;  // kKtThread: phase of an issued Kt MMA not yet observed complete
 
     if (nchunks > 0) {
         const int L0 = min(kChunk, eos - bos);
@@ -375,23 +392,24 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         {
             const int cp = ptid & 63, qt = ptid >> 6;
             const int ch = 2 * cp;
-            float d0[8], d1[8], e0[8], e1[8];
+            float d0[8], d1[8];
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 const int i = 8 * qt + ii;
-                d0[ii] = d1[ii] = e0[ii] = e1[ii] = 1.0f;
+                d0[ii] = d1[ii] = 1.0f;
                 if (i < L) {
                     float a0, a1;
                     unpack_bf16x2(*reinterpret_cast<const uint32_t *>(ra + 2 * (i * 128 + ch)), a0, a1);
-                    d0[ii] = gate_decay_pair(a0, a.gate_mode, a.lower_bound, e0[ii]);
-                    d1[ii] = gate_decay_pair(a1, a.gate_mode, a.lower_bound, e1[ii]);
+                    d0[ii] = gate_decay(a0, a.gate_mode, a.lower_bound);
+                    d1[ii] = gate_decay(a1, a.gate_mode, a.lower_bound);
                 }
             }
-            // P: inclusive prefix of d; S: exclusive suffix of d; F: the anchored factor made
-            // of 1/d (exclusive suffix up to the anchor in quarters 0 and 2, inclusive prefix
-            // from the anchor on in quarters 1 and 3).
+            // P: inclusive prefix of d; S: exclusive suffix of d. The anchored factor F is made
+            // of 1/d: the exclusive suffix of 1/d before the anchor (quarters 0 and 2), which
+            // is P / P_7, and the inclusive prefix of 1/d from the anchor on (quarters 1 and
+            // 3), which is S / P_7, so one reciprocal per channel serves the quarter.
             const bool before_anchor = (qt & 1) == 0;
-            float P0[8], P1[8], S0[8], S1[8], F0[8], F1[8];
+            float P0[8], P1[8], S0[8], S1[8];
             {
                 float r0 = 1.0f, r1 = 1.0f;
 #pragma unroll
@@ -409,25 +427,8 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     r0 *= d0[ii];
                     r1 *= d1[ii];
                 }
-                r0 = r1 = 1.0f;
-                if (before_anchor) {
-#pragma unroll
-                    for (int ii = 7; ii >= 0; --ii) {
-                        F0[ii] = r0;
-                        F1[ii] = r1;
-                        r0 *= e0[ii];
-                        r1 *= e1[ii];
-                    }
-                } else {
-#pragma unroll
-                    for (int ii = 0; ii < 8; ++ii) {
-                        r0 *= e0[ii];
-                        r1 *= e1[ii];
-                        F0[ii] = r0;
-                        F1[ii] = r1;
-                    }
-                }
             }
+            const float R0 = rcp(P0[7]), R1 = rcp(P1[7]);
             *reinterpret_cast<float2 *>(quart_s + qt * 128 + ch) = make_float2(P0[7], P1[7]);
             bar_named(kBarProd, kProdThreads);
             float2 T[4];
@@ -447,38 +448,52 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             // off-diagonal factors 2^(G_i - G_15) (i >= 16) and 2^(G_15 - G_j) (j < 16)
             const float od0 = (qt == 0) ? T[1].x : ((qt == 3) ? T[2].x : 1.0f);
             const float od1 = (qt == 0) ? T[1].y : ((qt == 3) ? T[2].y : 1.0f);
-            bool ok = true;
+            // the largest factors of the quarter: P_7 and 1/P_7 bound P, S and F when d <= 1,
+            // and F at its far end is checked directly for other gates
+            const float fmax0 = before_anchor ? P0[0] * R0 : R0, fmax1 = before_anchor ? P1[0] * R1 : R1;
+            if (!(fmax0 < 3.0e38f && fmax1 < 3.0e38f && R0 < 3.0e38f && R1 < 3.0e38f && P0[7] < 3.0e38f &&
+                  P1[7] < 3.0e38f))
+                report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
             float kr0[8], kr1[8];
+            // left factor fl (query / key rows of the diagonal blocks) and right factor fr
+            // (key columns): F and S before the anchor, P and F from it on
+            auto operands = [&](auto before) {
+                constexpr bool kBefore = decltype(before)::value;
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
-                const int i = 8 * qt + ii;
-                float k0, k1, q0, q1;
-                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rk + 2 * (i * 128 + ch)), k0, k1);
-                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rq + 2 * (i * 128 + ch)), q0, q1);
-                q0 *= a.scale;
-                q1 *= a.scale;
-                const float fl0 = before_anchor ? F0[ii] : P0[ii], fl1 = before_anchor ? F1[ii] : P1[ii];
-                const float fr0 = before_anchor ? S0[ii] : F0[ii], fr1 = before_anchor ? S1[ii] : F1[ii];
-                ok &= (fl0 < 3.0e38f) && (fl1 < 3.0e38f) && (fr0 < 3.0e38f) && (fr1 < 3.0e38f);
-                if (!kPass1) st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
-                st_pair(pairKL, i * kRowB + ch, k0 * fl0, k1 * fl1);
-                st_pair(pairKR, i * kRowB + ch, k0 * fr0, k1 * fr1);
-                if (qt >= 2) {
-                    const float fo0 = od0 * P0[ii], fo1 = od1 * P1[ii];
-                    if (!kPass1) st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
-                    st_pair(pairKL, (16 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
-                } else {
-                    const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
-                    st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                for (int ii = 0; ii < 8; ++ii) {
+                    const int i = 8 * qt + ii;
+                    float k0, k1, q0, q1;
+                    unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rk + 2 * (i * 128 + ch)), k0, k1);
+                    unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rq + 2 * (i * 128 + ch)), q0, q1);
+                    q0 *= a.scale;
+                    q1 *= a.scale;
+                    const float fl0 = kBefore ? P0[ii] * R0 : P0[ii], fl1 = kBefore ? P1[ii] * R1 : P1[ii];
+                    const float fr0 = kBefore ? S0[ii] : S0[ii] * R0, fr1 = kBefore ? S1[ii] : S1[ii] * R1;
+                    if (!kPass1) st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
+                    st_pair(pairKL, i * kRowB + ch, k0 * fl0, k1 * fl1);
+                    st_pair(pairKR, i * kRowB + ch, k0 * fr0, k1 * fr1);
+                    if (qt >= 2) {
+                        const float fo0 = od0 * P0[ii], fo1 = od1 * P1[ii];
+                        if (!kPass1) st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
+                        st_pair(pairKL, (16 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                    } else {
+                        const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
+                        st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                    }
+                    const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
+                    *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) =
+                        make_float2(tf32f(-k0 * fb0), tf32f(-k1 * fb1));
+                    if (!kPass1)
+                        *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) =
+                            make_float2(tf32f(q0 * fb0), tf32f(q1 * fb1));
+                    kr0[ii] = tf32f(k0 * (S0[ii] * post0));  // 2^(G_L - G_i)
+                    kr1[ii] = tf32f(k1 * (S1[ii] * post1));
                 }
-                const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
-                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) = make_float2(tf32f(-k0 * fb0), tf32f(-k1 * fb1));
-                if (!kPass1)
-                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) =
-                        make_float2(tf32f(q0 * fb0), tf32f(q1 * fb1));
-                kr0[ii] = __uint_as_float(to_tf32(k0 * (S0[ii] * post0)));  // 2^(G_L - G_i)
-                kr1[ii] = __uint_as_float(to_tf32(k1 * (S1[ii] * post1)));
-            }
+            };
+            if (before_anchor)
+                operands(std::true_type{});
+            else
+                operands(std::false_type{});
 #pragma unroll
             for (int h4 = 0; h4 < 2; ++h4) {
                 const int i0 = 8 * qt + 4 * h4;
@@ -487,7 +502,6 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch + 1, i0, 1024)) =
                     make_float4(kr1[4 * h4], kr1[4 * h4 + 1], kr1[4 * h4 + 2], kr1[4 * h4 + 3]);
             }
-            if (!ok) report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
             if (qt == 0)
                 *reinterpret_cast<float2 *>(stage + kStDec + 4 * ch) =
                     make_float2(T[0].x * T[1].x * T[2].x * T[3].x, T[0].y * T[1].y * T[2].y * T[3].y);
@@ -497,7 +511,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         //      its D1 buffer and beta aside, so the raw buffers can refill with chunk c + 1.
         {
             bool lost = c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status);
-            if (c >= 1 && ptid == 0) {
+            if (c >= 1 && ptid == kKtThread) {
                 lost = lost || !wait_or_abort(&B->kt, (c - 1) & 1, B, a.status);
                 kt_parity = -1;
             }
@@ -523,23 +537,39 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         }
         cp_async_commit();
 
-        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5).
-        //      The warps holding a diagonal block of N invert I + N there at once.
+        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5;
+        //      warps 6 and 7 take the second K half of the two diagonal N blocks). The warps
+        //      holding a diagonal block of N invert I + N there at once.
+        float *const npart = reinterpret_cast<float *>(smem + kNpart);
         if (warp < 6) {
           if (!(kPass1 && warp < 3)) {  // the Mqk blocks are not needed by the window pass
             const int which = warp / 3;
             const int blk = warp % 3;
+            const bool split = which == 1 && blk < 2;
             const uint8_t *Lb = which ? pairKL : pairQ;
             const int row0 = 16 * blk;
             float acc[2][4] = {};
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
+                if (split && ks >= 4) break;
                 uint32_t af[4], bfr[4];
                 ldsm_x4(af, smem_addr(Lb + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
                 ldsm_x4(bfr, smem_addr(pairKR + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
                                                   ((lane >> 3) & 1) * 8) * 2));
                 mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
                 mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
+            }
+            if (split) {
+                if (blk == 0)
+                    bar_named(kBarNpart, 64);
+                else
+                    bar_named(kBarNpart + 1, 64);
+                const float *pp = npart + (blk * 32 + lane) * 8;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[0][e] += pp[e];
+                    acc[1][e] += pp[4 + e];
+                }
             }
             const int oi = (blk == 0) ? 0 : 16;
             const int oj = (blk == 1) ? 16 : 0;
@@ -557,12 +587,30 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     }
                 }
             }
-            if (which == 1 && blk < 2) {
+            if (split) {
                 __syncwarp();
                 invert_diag16(nt_s, tinv, pscr + 64 * blk, 16 * blk, lane);
             }
           }
         } else {
+            const int blk = warp - 6, row0 = 16 * blk;
+            float acc[2][4] = {};
+#pragma unroll
+            for (int ks = 4; ks < 8; ++ks) {
+                uint32_t af[4], bfr[4];
+                ldsm_x4(af, smem_addr(pairKL + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
+                ldsm_x4(bfr, smem_addr(pairKR + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
+                                                  ((lane >> 3) & 1) * 8) * 2));
+                mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
+                mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
+            }
+            float *pp = npart + (blk * 32 + lane) * 8;
+            *reinterpret_cast<float4 *>(pp) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+            *reinterpret_cast<float4 *>(pp + 4) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+            if (blk == 0)
+                bar_arrive_named(kBarNpart, 64);
+            else
+                bar_arrive_named(kBarNpart + 1, 64);
             for (int idx = ptid - 192; idx < 256; idx += 64) {
                 const int i = idx >> 4, j = 16 + (idx & 15);
                 mq_s[i * kSq + j] = 0.0f;
@@ -609,7 +657,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
 
         // ---- 5. Kt^T = Kr^T T' on tcgen05 (M128 N32 K32, both operands in shared memory; read
         //      back at the next hand-off), and Bo = Mqk T' (output pass) by mma.sync TF32.
-        if (ptid == 0) {
+        if (ptid == kKtThread) {  // warp 2: its Bo tile is all zero
             tc_fence_after();
             const uint32_t kra = smem_addr(stage + kStKt), ah = smem_addr(at_hi), al = smem_addr(at_lo);
 #pragma unroll
@@ -647,11 +695,11 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         }
     }
     // an aborted loop may leave this thread's last Kt MMA unobserved: drain it (bounded)
-    if (aborted && ptid == 0 && kt_parity >= 0) mbar_wait(&B->kt, (uint32_t)kt_parity);
+    if (aborted && ptid == kKtThread && kt_parity >= 0) mbar_wait(&B->kt, (uint32_t)kt_parity);
     // hand-off of the last chunk
     if (!aborted && nchunks > 0) {
         const int c = nchunks - 1;
-        const bool lost = ptid == 0 && !wait_or_abort(&B->kt, c & 1, B, a.status);
+        const bool lost = ptid == kKtThread && !wait_or_abort(&B->kt, c & 1, B, a.status);
         if (!bar_any(kBarProd, kProdThreads, lost)) {
             tc_fence_after();
             kt_to_stage(tmem, smem + kStage0 + (c & 1) * kStageBytes, warp, lane);
@@ -839,7 +887,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
 constexpr uint32_t kColM = 128;
 constexpr uint32_t kColD1M = 320;
 __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int nchunks,
-                                 float *E_out, float *M_out) {
+                                 float *E_out, float *Mt_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;
     const int row = 32 * quad + lane;
@@ -916,16 +964,24 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
     if (bar_any(kBarState, kStateThreads, B->abort != 0)) return;
     if (nchunks > 0 && !wait_or_abort(&B->g2, (nchunks - 1) & 1, B, a.status)) return;
     tc_fence_after();
-    // E[dk][dv] from S^T (lane dv, column dk); M[dk][dk'] from M^T (lane dk', column dk)
+    // E[dk][dv] from S^T (lane dv, column dk); the map is stored transposed, M^T[dk'][dk],
+    // straight from its TMEM rows (lane dk', column dk), which is the order the carry reads.
 #pragma unroll 1
-    for (int j = 0; j < 16; ++j) {
-        const uint32_t col = (j < 8 ? kColS : kColM) + 16 * (j & 7);
-        float *dst = j < 8 ? E_out : M_out;
+    for (int j = 0; j < 8; ++j) {
         float v[16];
-        tmem_ld16(tmem + lane_base + col, v);
+        tmem_ld16(tmem + lane_base + kColS + 16 * j, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dst[(16 * (j & 7) + e) * kHeadDim + row] = v[e];
+        for (int e = 0; e < 16; ++e) E_out[(16 * j + e) * kHeadDim + row] = v[e];
+    }
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {
+        float v[16];
+        tmem_ld16(tmem + lane_base + kColM + 16 * j, v);
+        tmem_wait_ld();
+        float4 *dst = reinterpret_cast<float4 *>(Mt_out + (size_t)row * kHeadDim + 16 * j);
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) dst[e4] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
     }
 }
 
@@ -1029,57 +1085,76 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
 // ------------------------------------------------------------------ window carry
 //
 // S_start[w+1] = M_w S_start[w] + E_w for every window of a chain, in FP32 on CUDA cores.
-// The dv columns of S are independent, so each CTA carries 8 of them through all windows.
+// The dv columns of S are independent: each CTA carries 8 of them through all windows.
+// Warp p owns the 16 values of k in [16p, 16p + 16) and, per lane, 4 rows x 8 columns of
+// the product. The map arrives transposed (row k of M^T is column k of M), so a warp reads
+// 512 contiguous bytes per k; each register is refilled with the next window's value as
+// soon as this window's has been read. The 8 partial products are summed through shared
+// memory.
 constexpr int kCarryCols = 8;
-constexpr int kCarryThreads = 256;
+constexpr int kCarryWarps = kHeadDim / 16;
+constexpr int kCarryThreads = 32 * kCarryWarps;
 
 __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const PrefillArgs a) {
     __shared__ __align__(16) float S[kHeadDim][kCarryCols];
+    __shared__ __align__(16) float part[kCarryWarps][kCarryCols][kHeadDim];  // [slice][column][row]
     const int blocks = kHeadDim / kCarryCols;
     const int chain = blockIdx.x / blocks;
     const int c0 = (blockIdx.x - chain * blocks) * kCarryCols;
     const int n = chain / a.num_heads;
     const WindowSpan sp = window_span(a, n, 0);
     if (sp.wins_seq <= 1) return;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
     for (int idx = tid; idx < kHeadDim * kCarryCols; idx += kCarryThreads) {
         const int i = idx / kCarryCols, cc = idx % kCarryCols;
         S[i][cc] = a.init_state ? a.init_state[sbase + (size_t)i * kHeadDim + c0 + cc] : 0.0f;
     }
-    const int i = tid >> 1;          // output row
-    const int cq = (tid & 1) * 4;    // four of the block's columns
-    // Row i of every window map is read by this thread only; all 32 vectors of a row are
-    // requested at once, and the next window's row as soon as this window's FMAs are done.
-    float4 m4[kHeadDim / 4];
-    auto load_row = [&](int w) {
-        const float4 *M = reinterpret_cast<const float4 *>(window_slot(a, chain, w, 2) + (size_t)i * kHeadDim);
-#pragma unroll
-        for (int j = 0; j < kHeadDim / 4; ++j) m4[j] = __ldcg(M + j);
+    const int k0 = 16 * warp;
+    float4 mv[16];  // M^T[k0 + kk][4 lane .. 4 lane + 3]
+    auto map_row = [&](int w, int kk) {
+        return reinterpret_cast<const float4 *>(window_slot(a, chain, w, 2) + (size_t)(k0 + kk) * kHeadDim + 4 * lane);
     };
-    load_row(0);
+    // reduction / output thread: row ri, columns 4 ch .. 4 ch + 3
+    const int ri = tid & (kHeadDim - 1), ch = tid >> 7;
+    auto load_e = [&](int w) {
+        return __ldcg(reinterpret_cast<const float4 *>(window_slot(a, chain, w, 1) + (size_t)ri * kHeadDim + c0 + 4 * ch));
+    };
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) mv[kk] = __ldcg(map_row(0, kk));
+    float4 e4 = load_e(0);
     __syncthreads();
     for (int w = 0; w + 1 < sp.wins_seq; ++w) {
-        const float4 e4 = __ldcg(reinterpret_cast<const float4 *>(window_slot(a, chain, w, 1) + (size_t)i * kHeadDim +
-                                                                  c0 + cq));
-        float acc[4] = {e4.x, e4.y, e4.z, e4.w};
+        float acc[4][kCarryCols];
 #pragma unroll
-        for (int j = 0; j < kHeadDim / 4; ++j) {
-            const float mv[4] = {m4[j].x, m4[j].y, m4[j].z, m4[j].w};
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const float4 s4 = *reinterpret_cast<const float4 *>(&S[4 * j + jj][cq]);
-                acc[0] = fmaf(mv[jj], s4.x, acc[0]);
-                acc[1] = fmaf(mv[jj], s4.y, acc[1]);
-                acc[2] = fmaf(mv[jj], s4.z, acc[2]);
-                acc[3] = fmaf(mv[jj], s4.w, acc[3]);
-            }
+            for (int c = 0; c < kCarryCols; ++c) acc[r][c] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const float4 s0 = *reinterpret_cast<const float4 *>(&S[k0 + kk][0]);
+            const float4 s1 = *reinterpret_cast<const float4 *>(&S[k0 + kk][4]);
+            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            const float m[4] = {mv[kk].x, mv[kk].y, mv[kk].z, mv[kk].w};
+            if (w + 2 < sp.wins_seq) mv[kk] = __ldcg(map_row(w + 1, kk));  // next window's row, a step ahead
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < kCarryCols; ++c) acc[r][c] = fmaf(m[r], sv[c], acc[r][c]);
         }
-        if (w + 2 < sp.wins_seq) load_row(w + 1);
+#pragma unroll
+        for (int c = 0; c < kCarryCols; ++c)
+            *reinterpret_cast<float4 *>(&part[warp][c][4 * lane]) = make_float4(acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
         __syncthreads();
-        *reinterpret_cast<float4 *>(&S[i][cq]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4 *>(window_slot(a, chain, w + 1, 0) + (size_t)i * kHeadDim + c0 + cq) =
-            make_float4(acc[0], acc[1], acc[2], acc[3]);
+        float sum[4] = {e4.x, e4.y, e4.z, e4.w};
+        if (w + 2 < sp.wins_seq) e4 = load_e(w + 1);
+#pragma unroll
+        for (int p = 0; p < kCarryWarps; ++p)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sum[c] += part[p][4 * ch + c][ri];
+        const float4 s4 = make_float4(sum[0], sum[1], sum[2], sum[3]);
+        *reinterpret_cast<float4 *>(&S[ri][4 * ch]) = s4;
+        *reinterpret_cast<float4 *>(window_slot(a, chain, w + 1, 0) + (size_t)ri * kHeadDim + c0 + 4 * ch) = s4;
         __syncthreads();
     }
 }
