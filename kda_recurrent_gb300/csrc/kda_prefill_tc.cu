@@ -42,16 +42,19 @@
 namespace kda {
 namespace {
 
-constexpr int kProducerWarps = 8;
+constexpr int kProducerWarps = 8;  // group A: chunk operands and pair products
+constexpr int kSolveWarps = 4;     // group B: the WY inverse, Kt, Bo and the hand-off
 constexpr int kStateWarps = 4;
-constexpr int kFirstStateWarp = kProducerWarps;
-constexpr int kThreadsTc = (kProducerWarps + kStateWarps) * 32;
+constexpr int kFirstSolveWarp = kProducerWarps;
+constexpr int kFirstStateWarp = kProducerWarps + kSolveWarps;
+constexpr int kThreadsTc = (kProducerWarps + kSolveWarps + kStateWarps) * 32;
 constexpr int kProdThreads = kProducerWarps * 32;
+constexpr int kSolveThreads = kSolveWarps * 32;
 constexpr int kStateThreads = kStateWarps * 32;
-constexpr int kBarProd = 1;   // named barrier of the producer warps
+constexpr int kBarProd = 1;   // named barrier of group A
 constexpr int kBarState = 2;  // named barrier of the state warps
-constexpr int kBarNpart = 3;  // 3, 4: producer warp pairs (3, 6) and (4, 7) of the diagonal N blocks
-constexpr int kKtThread = 64; // producer thread that issues and observes the Kt MMA
+constexpr int kBarSolve = 3;  // named barrier of group B
+constexpr int kKtThread = (kFirstSolveWarp + 1) * 32;  // group B thread that issues and observes the Kt MMA
 
 constexpr int kRowB = 136;  // padded bf16 row stride (ldmatrix operands)
 constexpr int kSq = 36;     // fp32 32 x 32 tiles
@@ -77,19 +80,17 @@ constexpr int kPairQ = kPair;
 constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
 constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
 constexpr int kPairEnd = kPairKR + 48 * kRowB * 2;
+// Group B's work space (the diagonal inverse blocks form while group A refills the pairs).
 constexpr int kAtHi = kPairEnd;                   // tf32 [32][32] core matrices: T'^T, high part
-constexpr int kAtLo = kAtHi + 4096;               // tf32: T'^T minus the high part (read by the Kt
-                                                  //   MMA while the next chunk's pair operands form)
-constexpr int kTinv = kAtLo + 4096;               // fp32 [32][36]: (I + Diag(beta) A)^-1 (its diagonal
-constexpr int kPscr = kTinv + 32 * kSq * 4;       //   blocks form while Mqk still reads the pair operands);
-                                                  // fp32 [16][16]: N21 T11 (and 2 x [8][8] before)
-constexpr int kNpart = kPscr + 1024;              // fp32 [2][32 lanes][8]: second K half of the
-                                                  //   diagonal blocks of Diag(beta) A (mma fragments)
-constexpr int kNt = kNpart + 2048;                // fp32 [32][36]: (Diag(beta) A)^T
-constexpr int kMq = kNt + 32 * kSq * 4;           // fp32 [32][36]: Mqk
-constexpr int kQuart = kMq + 32 * kSq * 4;        // fp32 [4][128]: per-quarter decay products
-constexpr int kBetaS = kQuart + 4 * 128 * 4;      // fp32 [32]: beta of the chunk (raw copy is refilled early)
-constexpr int kOst = kBetaS + 128;                // bf16 [32][136]: output staging
+constexpr int kAtLo = kAtHi + 4096;               // tf32: T'^T minus the high part
+constexpr int kTinv = kAtLo + 4096;               // fp32 [32][36]: (I + Diag(beta) A)^-1
+constexpr int kPscr = kTinv + 32 * kSq * 4;       // fp32 [16][16]: N21 T11 (and 2 x [8][8] before)
+// Handed from group A to group B, one copy per chunk parity.
+constexpr int kNt = kPscr + 1024;                 // fp32 [2][32][36]: (Diag(beta) A)^T
+constexpr int kMq = kNt + 2 * 32 * kSq * 4;       // fp32 [2][32][36]: Mqk
+constexpr int kBetaS = kMq + 2 * 32 * kSq * 4;    // fp32 [2][32]: beta of the chunk
+constexpr int kQuart = kBetaS + 256;              // fp32 [4][128]: per-quarter decay products
+constexpr int kOst = kQuart + 4 * 128 * 4;        // bf16 [32][136]: output staging
 constexpr int kBars = kOst + 32 * kRowB * 2;
 constexpr int kSmemTc = kBars + 128;
 static_assert(kStage0 % 128 == 0 && kStageBytes % 128 == 0 && kAtHi % 128 == 0, "operand alignment");
@@ -106,13 +107,15 @@ constexpr uint32_t kIdescG2 = instr_desc(2, 128, 128);  // tf32, M128 N128
 constexpr uint32_t kIdescN32 = instr_desc(2, 128, 32);  // tf32, M128 N32
 
 struct Bars {
-    uint64_t prep[2];    // producers -> state warps: stage s filled (count kProdThreads)
+    uint64_t prep[2];    // group B -> state warps: stage s filled (count kSolveThreads)
     uint64_t g1;         // projection MMA complete (tcgen05.commit)
     uint64_t go;         // output MMA complete (tcgen05.commit)
     uint64_t g2;         // state update MMA complete (tcgen05.commit)
     uint64_t g2s[2];     // state update of a chunk on stage s complete (tcgen05.commit)
     uint64_t oread[2];   // D1 buffer b read out by the state warps (count kStateThreads)
-    uint64_t kt;         // producers' Kt MMA complete (tcgen05.commit)
+    uint64_t kt;         // group B's Kt MMA complete (tcgen05.commit)
+    uint64_t ab_full[2]; // group A -> B: chunk operands of parity p ready (count kProdThreads)
+    uint64_t ab_empty[2];// group B -> A: Mqk, N, beta of parity p consumed (count kSolveThreads)
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -120,10 +123,6 @@ static_assert(sizeof(Bars) <= 128, "barrier block");
 
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void bar_arrive_named(int id, int count) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Named-barrier sync of `count` threads that also returns, identically to all of them,
@@ -235,18 +234,20 @@ __device__ __forceinline__ void load_vb(const PrefillArgs &a, uint8_t *smem, int
 
 // ------------------------------------------------------------------ producers
 
-// Kt^T (TMEM lane = dk, column = token) -> the stage's Kt operand (tf32, [dk][token]).
-// Producer warps w and w + 4 share lane quadrant w % 4 and take 16 token columns each.
-__device__ __forceinline__ void kt_to_stage(uint32_t tmem, uint8_t *stage, int warp, int lane) {
-    const int quad = warp & 3, half = warp >> 2;
-    const int dk = 32 * quad + lane;
-    float v[16];
-    tmem_ld16(tmem + ((uint32_t)(32 * quad) << 16) + kColKt + 16 * half, v);
-    tmem_wait_ld();
+// Kt^T (TMEM lane = dk, column = token) -> the stage's Kt operand (tf32, [dk][token]), by
+// group B: its warp b owns lane quadrant b.
+__device__ __forceinline__ void kt_to_stage(uint32_t tmem, uint8_t *stage, int bwarp, int lane) {
+    const int dk = 32 * bwarp + lane;
 #pragma unroll
-    for (int e4 = 0; e4 < 4; ++e4)
-        *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(dk, 16 * half + 4 * e4, 1024)) =
-            make_float4(tf32f(v[4 * e4]), tf32f(v[4 * e4 + 1]), tf32f(v[4 * e4 + 2]), tf32f(v[4 * e4 + 3]));
+    for (int half = 0; half < 2; ++half) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * bwarp) << 16) + kColKt + 16 * half, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4)
+            *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(dk, 16 * half + 4 * e4, 1024)) =
+                make_float4(tf32f(v[4 * e4]), tf32f(v[4 * e4 + 1]), tf32f(v[4 * e4 + 2]), tf32f(v[4 * e4 + 3]));
+    }
 }
 
 // V^T of the chunk into its D1 buffer (lane = dv, column = token); the output pass also
@@ -339,6 +340,9 @@ __device__ __forceinline__ void invert_diag16(const float *nt, float *inv, float
     *reinterpret_cast<float2 *>(inv + (r0 + i) * kSq + o + j2) = make_float2(-q0, -q1);
 }
 
+// Group A, per chunk: the gate and decay factors, the chunk operands of the state MMAs
+// (stage), V^T into the chunk's D1 buffer, the raw loads of the next chunk, and the pair
+// products Mqk and Diag(beta) A for group B.
 template <bool kPass1>
 __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int n, int h, int bos,
                               int eos, int nchunks) {
@@ -348,21 +352,12 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     uint8_t *const pairQ = smem + kPairQ;
     uint8_t *const pairKL = smem + kPairKL;
     uint8_t *const pairKR = smem + kPairKR;
-    float *const tinv = reinterpret_cast<float *>(smem + kTinv);
-    float *const pscr = reinterpret_cast<float *>(smem + kPscr);
-    uint8_t *const at_hi = smem + kAtHi;
-    uint8_t *const at_lo = smem + kAtLo;
-    float *const nt_s = reinterpret_cast<float *>(smem + kNt);
-    float *const mq_s = reinterpret_cast<float *>(smem + kMq);
     float *const quart_s = reinterpret_cast<float *>(smem + kQuart);
     const uint8_t *const rq = smem + kRawQ;
     const uint8_t *const rk = smem + kRawK;
     const uint8_t *const ra = smem + kRawA;
     const uint8_t *const rv = smem + kRawV;
     const float *const rb = reinterpret_cast<const float *>(smem + kRawBeta);
-    float *const beta_s = reinterpret_cast<float *>(smem + kBetaS);
-    bool aborted = false;
-    int kt_parity = -1;  // kKtThread: phase of an issued Kt MMA not yet observed complete
 
     if (nchunks > 0) {
         const int L0 = min(kChunk, eos - bos);
@@ -376,14 +371,11 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         const int L = min(kChunk, eos - t0);
         const int ps = c & 1, db = c & 1;
         uint8_t *const stage = smem + kStage0 + ps * kStageBytes;
+        float *const nt_s = reinterpret_cast<float *>(smem + kNt) + ps * 32 * kSq;
+        float *const mq_s = reinterpret_cast<float *>(smem + kMq) + ps * 32 * kSq;
+        float *const beta_s = reinterpret_cast<float *>(smem + kBetaS) + ps * 32;
         cp_async_wait<0>();
-        {  // stage ps is free once the state update of chunk c - 2 has read it
-            const bool lost = c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status);
-            if (bar_any(kBarProd, kProdThreads, lost)) {
-                aborted = true;
-                break;
-            }
-        }
+        bar_named(kBarProd, kProdThreads);
 
         // ---- 1. decays, anchored factors, chunk operands. Thread = (channel pair, 8-token
         //      quarter). With d the per-token decay, every factor is a running product of d or
@@ -430,7 +422,13 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             }
             const float R0 = rcp(P0[7]), R1 = rcp(P1[7]);
             *reinterpret_cast<float2 *>(quart_s + qt * 128 + ch) = make_float2(P0[7], P1[7]);
-            bar_named(kBarProd, kProdThreads);
+            {  // the gate needs no shared state; before the stores: stage ps is free once the
+               // state update of chunk c - 2 has read it, the hand-off buffers of parity ps once
+               // group B is through with chunk c - 2
+                bool lost = c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status);
+                lost = lost || (c >= 2 && !wait_or_abort(&B->ab_empty[ps], ((c >> 1) + 1) & 1, B, a.status));
+                if (bar_any(kBarProd, kProdThreads, lost)) break;
+            }
             float2 T[4];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) T[q4] = *reinterpret_cast<const float2 *>(quart_s + q4 * 128 + ch);
@@ -457,43 +455,36 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             float kr0[8], kr1[8];
             // left factor fl (query / key rows of the diagonal blocks) and right factor fr
             // (key columns): F and S before the anchor, P and F from it on
-            auto operands = [&](auto before) {
-                constexpr bool kBefore = decltype(before)::value;
 #pragma unroll
-                for (int ii = 0; ii < 8; ++ii) {
-                    const int i = 8 * qt + ii;
-                    float k0, k1, q0, q1;
-                    unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rk + 2 * (i * 128 + ch)), k0, k1);
-                    unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rq + 2 * (i * 128 + ch)), q0, q1);
-                    q0 *= a.scale;
-                    q1 *= a.scale;
-                    const float fl0 = kBefore ? P0[ii] * R0 : P0[ii], fl1 = kBefore ? P1[ii] * R1 : P1[ii];
-                    const float fr0 = kBefore ? S0[ii] : S0[ii] * R0, fr1 = kBefore ? S1[ii] : S1[ii] * R1;
-                    if (!kPass1) st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
-                    st_pair(pairKL, i * kRowB + ch, k0 * fl0, k1 * fl1);
-                    st_pair(pairKR, i * kRowB + ch, k0 * fr0, k1 * fr1);
-                    if (qt >= 2) {
-                        const float fo0 = od0 * P0[ii], fo1 = od1 * P1[ii];
-                        if (!kPass1) st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
-                        st_pair(pairKL, (16 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
-                    } else {
-                        const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
-                        st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
-                    }
-                    const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
-                    *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) =
-                        make_float2(tf32f(-k0 * fb0), tf32f(-k1 * fb1));
-                    if (!kPass1)
-                        *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) =
-                            make_float2(tf32f(q0 * fb0), tf32f(q1 * fb1));
-                    kr0[ii] = tf32f(k0 * (S0[ii] * post0));  // 2^(G_L - G_i)
-                    kr1[ii] = tf32f(k1 * (S1[ii] * post1));
+            for (int ii = 0; ii < 8; ++ii) {
+                const int i = 8 * qt + ii;
+                float k0, k1, q0, q1;
+                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rk + 2 * (i * 128 + ch)), k0, k1);
+                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rq + 2 * (i * 128 + ch)), q0, q1);
+                q0 *= a.scale;
+                q1 *= a.scale;
+                const float fl0 = before_anchor ? P0[ii] * R0 : P0[ii], fl1 = before_anchor ? P1[ii] * R1 : P1[ii];
+                const float fr0 = before_anchor ? S0[ii] : S0[ii] * R0, fr1 = before_anchor ? S1[ii] : S1[ii] * R1;
+                if (!kPass1) st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
+                st_pair(pairKL, i * kRowB + ch, k0 * fl0, k1 * fl1);
+                st_pair(pairKR, i * kRowB + ch, k0 * fr0, k1 * fr1);
+                if (qt >= 2) {
+                    const float fo0 = od0 * P0[ii], fo1 = od1 * P1[ii];
+                    if (!kPass1) st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
+                    st_pair(pairKL, (16 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                } else {
+                    const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
+                    st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
                 }
-            };
-            if (before_anchor)
-                operands(std::true_type{});
-            else
-                operands(std::false_type{});
+                const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
+                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) =
+                    make_float2(tf32f(-k0 * fb0), tf32f(-k1 * fb1));
+                if (!kPass1)
+                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) =
+                        make_float2(tf32f(q0 * fb0), tf32f(q1 * fb1));
+                kr0[ii] = tf32f(k0 * (S0[ii] * post0));  // 2^(G_L - G_i)
+                kr1[ii] = tf32f(k1 * (S1[ii] * post1));
+            }
 #pragma unroll
             for (int h4 = 0; h4 < 2; ++h4) {
                 const int i0 = 8 * qt + 4 * h4;
@@ -506,29 +497,15 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 *reinterpret_cast<float2 *>(stage + kStDec + 4 * ch) =
                     make_float2(T[0].x * T[1].x * T[2].x * T[3].x, T[0].y * T[1].y * T[2].y * T[3].y);
         }
-        // ---- 1b. Hand-off of chunk c - 1 (its Kt MMA ran during phase 1): Kt into its stage in
-        //      place of Kr, then the stage is released to the state warps. V^T of chunk c into
-        //      its D1 buffer and beta aside, so the raw buffers can refill with chunk c + 1.
+        // ---- 1b. V^T of chunk c into its D1 buffer and beta aside, so the raw buffers can
+        //      refill with chunk c + 1.
         {
-            bool lost = c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status);
-            if (c >= 1 && ptid == kKtThread) {
-                lost = lost || !wait_or_abort(&B->kt, (c - 1) & 1, B, a.status);
-                kt_parity = -1;
-            }
-            if (bar_any(kBarProd, kProdThreads, lost)) {
-                aborted = true;
-                break;
-            }
+            const bool lost = c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status);
+            if (bar_any(kBarProd, kProdThreads, lost)) break;
         }
         tc_fence_after();
-        if (c >= 1) kt_to_stage(tmem, smem + kStage0 + (ps ^ 1) * kStageBytes, warp, lane);
         v_to_tmem<kPass1>(tmem, rv, db, warp, lane);
         if (ptid < kChunk) beta_s[ptid] = rb[ptid];
-        if (c >= 1) {
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(&B->prep[ps ^ 1]);
-        }
         bar_named(kBarProd, kProdThreads);
         if (c + 1 < nchunks) {
             const int t1 = t0 + kChunk;
@@ -537,39 +514,22 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         }
         cp_async_commit();
 
-        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5;
-        //      warps 6 and 7 take the second K half of the two diagonal N blocks). The warps
-        //      holding a diagonal block of N invert I + N there at once.
-        float *const npart = reinterpret_cast<float *>(smem + kNpart);
+        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5)
         if (warp < 6) {
           if (!(kPass1 && warp < 3)) {  // the Mqk blocks are not needed by the window pass
             const int which = warp / 3;
             const int blk = warp % 3;
-            const bool split = which == 1 && blk < 2;
             const uint8_t *Lb = which ? pairKL : pairQ;
             const int row0 = 16 * blk;
             float acc[2][4] = {};
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                if (split && ks >= 4) break;
                 uint32_t af[4], bfr[4];
                 ldsm_x4(af, smem_addr(Lb + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
                 ldsm_x4(bfr, smem_addr(pairKR + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
                                                   ((lane >> 3) & 1) * 8) * 2));
                 mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
                 mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
-            }
-            if (split) {
-                if (blk == 0)
-                    bar_named(kBarNpart, 64);
-                else
-                    bar_named(kBarNpart + 1, 64);
-                const float *pp = npart + (blk * 32 + lane) * 8;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[0][e] += pp[e];
-                    acc[1][e] += pp[4 + e];
-                }
             }
             const int oi = (blk == 0) ? 0 : 16;
             const int oj = (blk == 1) ? 16 : 0;
@@ -587,77 +547,106 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     }
                 }
             }
-            if (split) {
-                __syncwarp();
-                invert_diag16(nt_s, tinv, pscr + 64 * blk, 16 * blk, lane);
-            }
           }
+        } else if (!kPass1) {
+            for (int idx = ptid - 192; idx < 256; idx += 64)
+                mq_s[(idx >> 4) * kSq + 16 + (idx & 15)] = 0.0f;  // upper-right block of Mqk
+        }
+        // the stage operands, D1 and the pair products of chunk c go to group B
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&B->ab_full[ps]);
+    }
+    cp_async_wait<0>();
+}
+
+// Group B, per chunk: hand-off of the previous chunk (Kt read back into its stage, stage
+// released to the state warps), (I + Diag(beta) A)^-1 by 16 x 16 blocks, T' in two TF32
+// parts, the Kt MMA and Bo = Mqk T' (mma.sync TF32).
+template <bool kPass1>
+__device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int nchunks) {
+    const int btid = threadIdx.x - kFirstSolveWarp * 32;  // 0 .. 127
+    const int bwarp = btid >> 5, lane = btid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const bool kt_thread = threadIdx.x == kKtThread;
+    float *const tinv = reinterpret_cast<float *>(smem + kTinv);
+    float *const pscr = reinterpret_cast<float *>(smem + kPscr);
+    uint8_t *const at_hi = smem + kAtHi;
+    uint8_t *const at_lo = smem + kAtLo;
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int ps = c & 1;
+        uint8_t *const stage = smem + kStage0 + ps * kStageBytes;
+        const float *const nt_s = reinterpret_cast<const float *>(smem + kNt) + ps * 32 * kSq;
+        const float *const mq_s = reinterpret_cast<const float *>(smem + kMq) + ps * 32 * kSq;
+        const float *const beta_s = reinterpret_cast<const float *>(smem + kBetaS) + ps * 32;
+        {
+            const bool lost = !wait_or_abort(&B->ab_full[ps], (c >> 1) & 1, B, a.status);
+            if (bar_any(kBarSolve, kSolveThreads, lost)) break;
+        }
+        tc_fence_after();
+
+        // ---- T = (I + N)^-1, N = Diag(beta) A strictly lower triangular, in FP32 by 16 x 16
+        //      blocks: the diagonal blocks (warps 0, 1), then T21 = -T22 N21 T11.
+        if (bwarp < 2) {
+            invert_diag16(nt_s, tinv, pscr + 64 * bwarp, 16 * bwarp, lane);
         } else {
-            const int blk = warp - 6, row0 = 16 * blk;
-            float acc[2][4] = {};
+            for (int idx = btid - 64; idx < 256; idx += 64)
+                tinv[(idx >> 4) * kSq + 16 + (idx & 15)] = 0.0f;  // upper-right block
+        }
+        bar_named(kBarSolve, kSolveThreads);
+        {
+            const int i = btid >> 3, j2 = 2 * (btid & 7);
+            float p0 = 0.0f, p1 = 0.0f;
 #pragma unroll
-            for (int ks = 4; ks < 8; ++ks) {
-                uint32_t af[4], bfr[4];
-                ldsm_x4(af, smem_addr(pairKL + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
-                ldsm_x4(bfr, smem_addr(pairKR + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
-                                                  ((lane >> 3) & 1) * 8) * 2));
-                mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
-                mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
+            for (int l = 0; l < 16; ++l) {
+                const float nv = nt_s[l * kSq + 16 + i];
+                const float2 tv = *reinterpret_cast<const float2 *>(tinv + l * kSq + j2);
+                p0 = fmaf(nv, tv.x, p0);
+                p1 = fmaf(nv, tv.y, p1);
             }
-            float *pp = npart + (blk * 32 + lane) * 8;
-            *reinterpret_cast<float4 *>(pp) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-            *reinterpret_cast<float4 *>(pp + 4) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-            if (blk == 0)
-                bar_arrive_named(kBarNpart, 64);
-            else
-                bar_arrive_named(kBarNpart + 1, 64);
-            for (int idx = ptid - 192; idx < 256; idx += 64) {
-                const int i = idx >> 4, j = 16 + (idx & 15);
-                mq_s[i * kSq + j] = 0.0f;
-                tinv[i * kSq + j] = 0.0f;  // upper-right block of the inverse
+            *reinterpret_cast<float2 *>(pscr + i * 16 + j2) = make_float2(p0, p1);
+        }
+        bar_named(kBarSolve, kSolveThreads);
+        {
+            const int i = btid >> 3, j2 = 2 * (btid & 7);
+            float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float tv = tinv[(16 + i) * kSq + 16 + k];
+                const float2 pv = *reinterpret_cast<const float2 *>(pscr + k * 16 + j2);
+                p0 = fmaf(tv, pv.x, p0);
+                p1 = fmaf(tv, pv.y, p1);
             }
+            *reinterpret_cast<float2 *>(tinv + (16 + i) * kSq + j2) = make_float2(-p0, -p1);
         }
-        bar_named(kBarProd, kProdThreads);
+        bar_named(kBarSolve, kSolveThreads);
 
-        // ---- 3. off-diagonal block of the inverse: T21 = -T22 N21 T11
+        // ---- T' = T Diag(beta), stored as T'^T (row j, K index i) in two TF32 parts
         {
-            const int i = ptid >> 4, j = ptid & 15;
-            float p = 0.0f;
-#pragma unroll
-            for (int l = 0; l < 16; ++l) p = fmaf(nt_s[l * kSq + 16 + i], tinv[l * kSq + j], p);
-            pscr[i * 16 + j] = p;
-        }
-        bar_named(kBarProd, kProdThreads);
-        {
-            const int i = ptid >> 4, j = ptid & 15;
-            float p = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) p = fmaf(tinv[(16 + i) * kSq + 16 + k], pscr[k * 16 + j], p);
-            tinv[(16 + i) * kSq + j] = -p;
-        }
-        bar_named(kBarProd, kProdThreads);
-
-        // ---- 4. T' = T Diag(beta), stored as T'^T (row j, K index i) in two TF32 parts
-        {
-            const int j = ptid & 31, q = ptid >> 5;  // T'[4q .. 4q + 3][j]
+            const int j = btid & 31;
             const float bj = beta_s[j];
-            float hi[4], lo[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float x = tinv[(4 * q + r) * kSq + j] * bj;
-                hi[r] = tf32f(x);
-                lo[r] = tf32f(x - hi[r]);
+            for (int qh = 0; qh < 2; ++qh) {
+                const int q = (btid >> 5) + 4 * qh;  // T'[4q .. 4q + 3][j]
+                float hi[4], lo[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float x = tinv[(4 * q + r) * kSq + j] * bj;
+                    hi[r] = tf32f(x);
+                    lo[r] = tf32f(x - hi[r]);
+                }
+                const int off = core_off_tf32(j, 4 * q, 1024);
+                *reinterpret_cast<float4 *>(at_hi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(at_lo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
-            const int off = core_off_tf32(j, 4 * q, 1024);
-            *reinterpret_cast<float4 *>(at_hi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4 *>(at_lo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
         }
         fence_async_smem();
-        bar_named(kBarProd, kProdThreads);
+        bar_named(kBarSolve, kSolveThreads);
 
-        // ---- 5. Kt^T = Kr^T T' on tcgen05 (M128 N32 K32, both operands in shared memory; read
+        // ---- Kt^T = Kr^T T' on tcgen05 (M128 N32 K32, both operands in shared memory; read
         //      back at the next hand-off), and Bo = Mqk T' (output pass) by mma.sync TF32.
-        if (ptid == kKtThread) {  // warp 2: its Bo tile is all zero
+        if (kt_thread) {  // warp 1: its Bo tiles are all zero
             tc_fence_after();
             const uint32_t kra = smem_addr(stage + kStKt), ah = smem_addr(at_hi), al = smem_addr(at_lo);
 #pragma unroll
@@ -669,46 +658,46 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 mma_tf32_ss(tmem + kColKt, smem_desc_kmajor(kra + 256 * s, 128, 1024),
                             smem_desc_kmajor(al + 256 * s, 128, 1024), kIdescN32, true);
             mma_commit(&B->kt);
-            kt_parity = c & 1;
         }
         __syncwarp();
         if (!kPass1) {
-            // warp = one 16 x 8 tile of Bo; Bo is lower triangular, so K steps outside
-            // [column tile, row tile] contribute nothing
-            const int mt = warp >> 2, nt = warp & 3;
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // warp b: the 16 x 8 tiles (b / 2, 2 (b % 2)) and (b / 2, 2 (b % 2) + 1) of Bo; Bo is
+            // lower triangular, so K steps outside [column tile, row tile] contribute nothing
+            const int mt = bwarp >> 1;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                if (ks < nt || ks > 2 * mt + 1) continue;
-                const int r0 = 16 * mt + g, k0 = 8 * ks + t4;
-                const uint32_t af[4] = {to_tf32(mq_s[r0 * kSq + k0]), to_tf32(mq_s[(r0 + 8) * kSq + k0]),
-                                        to_tf32(mq_s[r0 * kSq + k0 + 4]), to_tf32(mq_s[(r0 + 8) * kSq + k0 + 4])};
-                const int jn = 8 * nt + g;
-                const float bj = beta_s[jn];
-                mma_tf32_1688(acc, af, to_tf32(tinv[k0 * kSq + jn] * bj), to_tf32(tinv[(k0 + 4) * kSq + jn] * bj));
+            for (int u = 0; u < 2; ++u) {
+                const int nt = 2 * (bwarp & 1) + u;
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    if (ks < nt || ks > 2 * mt + 1) continue;
+                    const int r0 = 16 * mt + g, k0 = 8 * ks + t4;
+                    const uint32_t af[4] = {to_tf32(mq_s[r0 * kSq + k0]), to_tf32(mq_s[(r0 + 8) * kSq + k0]),
+                                            to_tf32(mq_s[r0 * kSq + k0 + 4]), to_tf32(mq_s[(r0 + 8) * kSq + k0 + 4])};
+                    const int jn = 8 * nt + g;
+                    const float bj = beta_s[jn];
+                    mma_tf32_1688(acc, af, to_tf32(tinv[k0 * kSq + jn] * bj),
+                                  to_tf32(tinv[(k0 + 4) * kSq + jn] * bj));
+                }
+                const int i0 = 16 * mt + g, j0 = 8 * nt + 2 * t4;
+                *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0, j0, 1024)) =
+                    make_float2(tf32f(acc[0]), tf32f(acc[1]));
+                *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0 + 8, j0, 1024)) =
+                    make_float2(tf32f(acc[2]), tf32f(acc[3]));
             }
-            const int i0 = 16 * mt + g, j0 = 8 * nt + 2 * t4;
-            *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0, j0, 1024)) =
-                make_float2(tf32f(acc[0]), tf32f(acc[1]));
-            *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0 + 8, j0, 1024)) =
-                make_float2(tf32f(acc[2]), tf32f(acc[3]));
         }
-    }
-    // an aborted loop may leave this thread's last Kt MMA unobserved: drain it (bounded)
-    if (aborted && ptid == kKtThread && kt_parity >= 0) mbar_wait(&B->kt, (uint32_t)kt_parity);
-    // hand-off of the last chunk
-    if (!aborted && nchunks > 0) {
-        const int c = nchunks - 1;
-        const bool lost = ptid == kKtThread && !wait_or_abort(&B->kt, c & 1, B, a.status);
-        if (!bar_any(kBarProd, kProdThreads, lost)) {
-            tc_fence_after();
-            kt_to_stage(tmem, smem + kStage0 + (c & 1) * kStageBytes, warp, lane);
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(&B->prep[c & 1]);
+        mbar_arrive(&B->ab_empty[ps]);
+        // ---- hand-off: Kt in place of Kr, then the stage goes to the state warps
+        {
+            const bool lost = kt_thread && !wait_or_abort(&B->kt, c & 1, B, a.status);
+            if (bar_any(kBarSolve, kSolveThreads, lost)) break;
         }
+        tc_fence_after();
+        kt_to_stage(tmem, stage, bwarp, lane);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&B->prep[ps]);
     }
-    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------ state warps
@@ -739,9 +728,33 @@ __device__ __forceinline__ void store_state(uint32_t tmem_state, uint32_t lane_b
     }
 }
 
+// dst[col] = src[col] * dec[col % 128] over `blocks` blocks of 32 columns of this thread's TMEM
+// lane; the load of the next block is in flight while the current one is scaled and stored.
+__device__ __forceinline__ void decay_columns(uint32_t src, uint32_t dst, const float *dec, int blocks) {
+    float v[2][32];
+    tmem_ld32(src, v[0]);
+#pragma unroll 1
+    for (int j = 0; j < blocks; j += 2) {
+        tmem_wait_ld();
+        if (j + 1 < blocks) tmem_ld32(src + 32 * (j + 1), v[1]);
+        const float *d0 = dec + ((32 * j) & 127);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[0][e] *= d0[e];
+        tmem_st32(dst + 32 * j, v[0]);
+        if (j + 1 >= blocks) break;
+        tmem_wait_ld();
+        if (j + 2 < blocks) tmem_ld32(src + 32 * (j + 2), v[0]);
+        const float *d1 = dec + ((32 * (j + 1)) & 127);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[1][e] *= d1[e];
+        tmem_st32(dst + 32 * (j + 1), v[1]);
+    }
+    tmem_wait_st();
+}
+
 __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int n, int h, int bos,
                            int eos, int nchunks, int chunk_base, const float *init, float *fin_out) {
-    const int stid = threadIdx.x - kProdThreads;  // 0 .. 127
+    const int stid = threadIdx.x - kFirstStateWarp * 32;  // 0 .. 127
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;
     const int dv = 32 * quad + lane;
@@ -787,19 +800,8 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                             a.ckpt + ((size_t)row * a.num_heads + h) * (kHeadDim * kHeadDim));
         }
         // decay into the other state buffer while the projection reads this one
-        {
-            const float *dec = reinterpret_cast<const float *>(stage + kStDec);
-#pragma unroll 1
-            for (int j = 0; j < 8; ++j) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + cur + 16 * j, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= dec[16 * j + e];
-                tmem_st16(tmem + lane_base + nxt + 16 * j, v);
-            }
-            tmem_wait_st();
-        }
+        decay_columns(tmem + lane_base + cur, tmem + lane_base + nxt, reinterpret_cast<const float *>(stage + kStDec),
+                      4);
         tc_fence_before();
         bar_named(kBarState, kStateThreads);
         tc_fence_after();
@@ -929,20 +931,9 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         __syncwarp();
         if (!wait_or_abort(&B->g1, c & 1, B, a.status)) break;
         tc_fence_after();
-        {
-            const float *dec = reinterpret_cast<const float *>(stage + kStDec);
-#pragma unroll 1
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t col = (j < 8 ? kColS : kColM) + 16 * (j & 7);
-                float v[16];
-                tmem_ld16(tmem + lane_base + col, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= dec[16 * (j & 7) + e];
-                tmem_st16(tmem + lane_base + col, v);
-            }
-            tmem_wait_st();
-        }
+        // S and M are adjacent (columns [0, 256)): decay both in place
+        decay_columns(tmem + lane_base + kColS, tmem + lane_base + kColS, reinterpret_cast<const float *>(stage + kStDec),
+                      8);
         tc_fence_before();
         mbar_arrive(&B->oread[db]);
         bar_named(kBarState, kStateThreads);
@@ -1035,8 +1026,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     const int nchunks = (eos - bos + kChunk - 1) / kChunk;
 
     if (threadIdx.x == 0) {
-        mbar_init(&B->prep[0], kProdThreads);
-        mbar_init(&B->prep[1], kProdThreads);
+        mbar_init(&B->prep[0], kSolveThreads);
+        mbar_init(&B->prep[1], kSolveThreads);
+        mbar_init(&B->ab_full[0], kProdThreads);
+        mbar_init(&B->ab_full[1], kProdThreads);
+        mbar_init(&B->ab_empty[0], kSolveThreads);
+        mbar_init(&B->ab_empty[1], kSolveThreads);
         mbar_init(&B->g1, 1);
         mbar_init(&B->go, 1);
         mbar_init(&B->kt, 1);
@@ -1059,6 +1054,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
 
     if (warp < kProducerWarps) {
         producer_loop<kPass1>(a, smem, B, tmem, n, h, bos, eos, nchunks);
+    } else if (warp < kFirstStateWarp) {
+        solve_loop<kPass1>(a, smem, B, tmem, nchunks);
     } else {
         if (kPass1) {
             state_loop_pass1(a, smem, B, tmem, nchunks, window_slot(a, chain, w, 1), window_slot(a, chain, w, 2));
