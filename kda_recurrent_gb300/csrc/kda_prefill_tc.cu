@@ -16,8 +16,7 @@
 //     S_nxt = S_cur Diag(2^G_last)                                  (state warps, TMEM -> TMEM)
 //     S_nxt^T += R^T Kt             M128 N128 K32, A = R^T read from TMEM
 // Kt^T = Kr^T T' is one more small tcgen05 product (M128 N32 K32, both operands in shared
-// memory, T' split into two TF32 terms so the product keeps FP32 accuracy), issued by the
-// producers off the serial chain. The state is ping-ponged between two TMEM buffers so that
+// memory, TF32), issued by the producers off the serial chain. The state is ping-ponged between two TMEM buffers so that
 // the decay runs while the projection reads the previous buffer.
 //
 // Warp roles (one CTA per (sequence, head) chain, 12 warps):
@@ -81,9 +80,8 @@ constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
 constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
 constexpr int kPairEnd = kPairKR + 48 * kRowB * 2;
 // Group B's work space (the diagonal inverse blocks form while group A refills the pairs).
-constexpr int kAtHi = kPairEnd;                   // tf32 [32][32] core matrices: T'^T, high part
-constexpr int kAtLo = kAtHi + 4096;               // tf32: T'^T minus the high part
-constexpr int kTinv = kAtLo + 4096;               // fp32 [32][36]: (I + Diag(beta) A)^-1
+constexpr int kAtHi = kPairEnd;                   // tf32 [32][32] core matrices: T'^T
+constexpr int kTinv = kAtHi + 4096;               // fp32 [32][36]: (I + Diag(beta) A)^-1
 constexpr int kPscr = kTinv + 32 * kSq * 4;       // fp32 [16][16]: N21 T11 (and 2 x [8][8] before)
 // Handed from group A to group B, one copy per chunk parity.
 constexpr int kNt = kPscr + 1024;                 // fp32 [2][32][36]: (Diag(beta) A)^T
@@ -560,9 +558,9 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     cp_async_wait<0>();
 }
 
-// Group B, per chunk: hand-off of the previous chunk (Kt read back into its stage, stage
-// released to the state warps), (I + Diag(beta) A)^-1 by 16 x 16 blocks, T' in two TF32
-// parts, the Kt MMA and Bo = Mqk T' (mma.sync TF32).
+// Group B, per chunk: (I + Diag(beta) A)^-1 by 16 x 16 blocks, T' in TF32, the Kt MMA and
+// Bo = Mqk T' (mma.sync TF32) while it runs, then the hand-off: Kt read back into the stage
+// in place of Kr, and the stage released to the state warps.
 template <bool kPass1>
 __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int nchunks) {
     const int btid = threadIdx.x - kFirstSolveWarp * 32;  // 0 .. 127
@@ -572,7 +570,6 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
     float *const tinv = reinterpret_cast<float *>(smem + kTinv);
     float *const pscr = reinterpret_cast<float *>(smem + kPscr);
     uint8_t *const at_hi = smem + kAtHi;
-    uint8_t *const at_lo = smem + kAtLo;
 
     for (int c = 0; c < nchunks; ++c) {
         const int ps = c & 1;
@@ -622,41 +619,33 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         }
         bar_named(kBarSolve, kSolveThreads);
 
-        // ---- T' = T Diag(beta), stored as T'^T (row j, K index i) in two TF32 parts
+        // ---- T' = T Diag(beta), stored as T'^T (row j, K index i) in TF32
         {
             const int j = btid & 31;
             const float bj = beta_s[j];
 #pragma unroll
             for (int qh = 0; qh < 2; ++qh) {
                 const int q = (btid >> 5) + 4 * qh;  // T'[4q .. 4q + 3][j]
-                float hi[4], lo[4];
+                float hi[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const float x = tinv[(4 * q + r) * kSq + j] * bj;
-                    hi[r] = tf32f(x);
-                    lo[r] = tf32f(x - hi[r]);
-                }
+                for (int r = 0; r < 4; ++r) hi[r] = tf32f(tinv[(4 * q + r) * kSq + j] * bj);
                 const int off = core_off_tf32(j, 4 * q, 1024);
                 *reinterpret_cast<float4 *>(at_hi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4 *>(at_lo + off) = make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         fence_async_smem();
         bar_named(kBarSolve, kSolveThreads);
 
         // ---- Kt^T = Kr^T T' on tcgen05 (M128 N32 K32, both operands in shared memory; read
-        //      back at the next hand-off), and Bo = Mqk T' (output pass) by mma.sync TF32.
+        //      back at the hand-off below), and Bo = Mqk T' (output pass) by mma.sync TF32.
         if (kt_thread) {  // warp 1: its Bo tiles are all zero
             tc_fence_after();
-            const uint32_t kra = smem_addr(stage + kStKt), ah = smem_addr(at_hi), al = smem_addr(at_lo);
+            const uint32_t kra = smem_addr(stage + kStKt), ah = smem_addr(at_hi);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_tf32_ss(tmem + kColKt, smem_desc_kmajor(kra + 256 * s, 128, 1024),
                             smem_desc_kmajor(ah + 256 * s, 128, 1024), kIdescN32, s > 0);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_tf32_ss(tmem + kColKt, smem_desc_kmajor(kra + 256 * s, 128, 1024),
-                            smem_desc_kmajor(al + 256 * s, 128, 1024), kIdescN32, true);
+
             mma_commit(&B->kt);
         }
         __syncwarp();
