@@ -358,61 +358,95 @@ def run_ours(args):
 
 
 def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws):
-    """Same metric through the C ABI from pinned host buffers: H2D of the step's inputs,
-    the two calls, D2H of the outputs (prefill out + final state, decode out)."""
+    """Same metric through the C ABI from pinned host buffers, every step's inputs copied in
+    and its results (prefill out + final state, decode out) copied back inside the timed
+    region. Steps are pipelined over three streams, as a serving loop would run them: the
+    H2D copy of step s+1 and the D2H copy of step s-1 overlap the kernels of step s, with
+    two device copies of every input and output."""
     import torch
     host_p = {k: (v.to("cpu").pin_memory() if v is not None else None) for k, v in pin.items()}
     host_d = {k: v.to("cpu").pin_memory() for k, v in din.items()}
-    dev_p = {k: (torch.empty_like(v, device=device) if v is not None else None) for k, v in host_p.items()}
-    dev_d = {k: torch.empty_like(v, device=device) for k, v in host_d.items()}
-    out = torch.empty_like(dev_p["q"])
-    fin = torch.empty(len(pcfg.seqlens), pcfg.num_heads, 128, 128, dtype=torch.float32, device=device)
-    dout = torch.empty_like(dev_d["q"])
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
-    h_dout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    dev_p = [{k: (torch.empty_like(v, device=device) if v is not None else None) for k, v in host_p.items()}
+             for _ in range(2)]
+    dev_d = [{k: torch.empty_like(v, device=device) for k, v in host_d.items()} for _ in range(2)]
+    out = [torch.empty_like(dev_p[0]["q"]) for _ in range(2)]
+    fin = [torch.empty(len(pcfg.seqlens), pcfg.num_heads, 128, 128, dtype=torch.float32, device=device)
+           for _ in range(2)]
+    dout = [torch.empty_like(dev_d[0]["q"]) for _ in range(2)]
+    h_out = [torch.empty(out[0].shape, dtype=out[0].dtype).pin_memory() for _ in range(2)]
+    h_fin = [torch.empty(fin[0].shape, dtype=fin[0].dtype).pin_memory() for _ in range(2)]
+    h_dout = [torch.empty(dout[0].shape, dtype=dout[0].dtype).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_p.values() if v is not None)
     h2d_d = sum(v.numel() * v.element_size() for v in host_d.values())
-    d2h = h_out.numel() * 2 + h_fin.numel() * 4
-    d2h_d = h_dout.numel() * 2
+    d2h = h_out[0].numel() * 2 + h_fin[0].numel() * 4
+    d2h_d = h_dout[0].numel() * 2
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
-    def step():
+    def pipeline(nsteps, copy_in, compute, copy_out):
+        """Runs nsteps pipelined steps; returns the CUDA-event time from the first copy in to
+        the last copy out, in ms."""
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        in_done, comp_done, out_done = [ev() for _ in range(nsteps)], [ev() for _ in range(nsteps)], [ev() for _ in range(nsteps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for i in range(nsteps):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])  # buffer b's inputs are read
+                copy_in(b)
+                in_done[i].record(s_in)
+            stream.wait_event(in_done[i])
+            if i >= 2:
+                stream.wait_event(out_done[i - 2])  # buffer b's outputs are copied out
+            compute(b)
+            comp_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                copy_out(b)
+                out_done[i].record(s_out)
+        t1.record(s_out)
+        torch.cuda.synchronize(device)
+        return t0.elapsed_time(t1)
+
+    def p_in(b):
         for k2, v in host_p.items():
             if v is not None:
-                dev_p[k2].copy_(v, non_blocking=True)
-        K.kda_prefill_ex(dev_p["q"], dev_p["k"], dev_p["v"], dev_p["g_raw"], dev_p["beta"], dev_p["cu_seqlens"],
-                         dev_p["init_state"], out, fin, pcfg.scale, pcfg.lower_bound, pcfg.gate_mode, ws, stream)
-        h_out.copy_(out, non_blocking=True)
-        h_fin.copy_(fin, non_blocking=True)
+                dev_p[b][k2].copy_(v, non_blocking=True)
 
-    def dstep():
+    def p_comp(b):
+        d = dev_p[b]
+        K.kda_prefill_ex(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], d["cu_seqlens"], d["init_state"], out[b],
+                         fin[b], pcfg.scale, pcfg.lower_bound, pcfg.gate_mode, ws, stream)
+
+    def p_out(b):
+        h_out[b].copy_(out[b], non_blocking=True)
+        h_fin[b].copy_(fin[b], non_blocking=True)
+
+    def d_in(b):
         for k2, v in host_d.items():
-            dev_d[k2].copy_(v, non_blocking=True)
-        K.kda_decode(dev_d["q"], dev_d["k"], dev_d["v"], dev_d["g_raw"], dev_d["beta"], dev_d["slot_idx"], pool, dout,
-                     dcfg.scale, dcfg.lower_bound, dcfg.gate_mode, stream)
-        h_dout.copy_(dout, non_blocking=True)
+            dev_d[b][k2].copy_(v, non_blocking=True)
 
-    for _ in range(max(1, args.warmup // 2)):
-        step()
-        dstep()
-    torch.cuda.synchronize(device)
+    def d_comp(b):
+        d = dev_d[b]
+        K.kda_decode(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], d["slot_idx"], pool, dout[b], dcfg.scale,
+                     dcfg.lower_bound, dcfg.gate_mode, stream)
+
+    def d_out(b):
+        h_dout[b].copy_(dout[b], non_blocking=True)
+
     steps = max(3, args.steps // 2)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    for s in range(steps):
-        ev[s][0].record(stream)
-        step()
-        ev[s][1].record(stream)
-        dstep()
-        ev[s][2].record(stream)
-    torch.cuda.synchronize(device)
-    p_ms = max_over_ranks(sum(ev[s][0].elapsed_time(ev[s][1]) for s in range(steps)) / steps, dist, device)
-    d_ms = max_over_ranks(sum(ev[s][1].elapsed_time(ev[s][2]) for s in range(steps)) / steps, dist, device)
+    pipeline(max(2, args.warmup), p_in, p_comp, p_out)  # warm-up
+    p_ms = max_over_ranks(pipeline(steps, p_in, p_comp, p_out) / steps, dist, device)
+    pipeline(max(2, args.warmup), d_in, d_comp, d_out)
+    d_ms = max_over_ranks(pipeline(steps, d_in, d_comp, d_out) / steps, dist, device)
     world = dist.get_world_size() if dist is not None else 1
     return {"value": round(prefill_units(pcfg) * world / (p_ms * 1e-3), 1), "unit": "tokens*heads/s",
             "h2d_bytes_per_step": int(h2d + h2d_d), "d2h_bytes_per_step": int(d2h + d2h_d),
             "prefill_ms": round(p_ms, 4), "decode_ms": round(d_ms, 4),
             "decode_value": round(args.decode_rows * dcfg.num_heads * world / (d_ms * 1e-3), 1),
-            "decode_unit": "rows*heads/s"}
+            "decode_unit": "rows*heads/s", "schedule": "H2D, kernels and D2H of consecutive steps overlap "
+            "on three streams; two device copies of inputs and outputs"}
 
 
 def decode_kernel_name(items: int, sms: int) -> str:
