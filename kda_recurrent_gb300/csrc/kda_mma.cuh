@@ -20,11 +20,14 @@ __device__ __forceinline__ float bf16_round(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// FP32 -> TF32 (round to nearest, ties away), returned as the 32-bit pattern mma expects.
+// FP32 -> TF32 (round to nearest, ties away from zero), returned as the 32-bit pattern the
+// tensor cores read. Done on the integer pipe: half a TF32 ulp (bit 12) is added to the
+// magnitude bits and the 13 bits below the TF32 mantissa are cleared; a carry into the
+// exponent is the correct rounding up. Finite inputs round as the TF32 conversion does,
+// infinities and quiet NaNs are kept; a NaN whose payload lies only in the low 13 bits
+// becomes an infinity. The conversion instruction costs more here under full load.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
