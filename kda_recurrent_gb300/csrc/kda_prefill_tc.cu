@@ -62,10 +62,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---- shared-memory map (bytes)
 constexpr int kRawQ = 0;                          // bf16 [32][128]
 constexpr int kRawK = kRawQ + 8192;
-constexpr int kRawA = kRawK + 8192;
-constexpr int kRawV = kRawA + 8192;               // bf16 [32][136]
-constexpr int kRawBeta = kRawV + 32 * kRowB * 2;  // fp32 [32]
-constexpr int kStage0 = kRawBeta + 128;
+constexpr int kRawA = kRawK + 8192;               // bf16 [2][32][128]: the gate tile, two chunks ahead
+constexpr int kRawV = kRawA + 2 * 8192;           // bf16 [2][32][136]: v, one buffer per chunk parity
+constexpr int kRawVBytes = 32 * kRowB * 2;
+constexpr int kRawBeta = kRawV + 2 * kRawVBytes;  // fp32 [2][32]: beta, one buffer per chunk parity
+constexpr int kStage0 = kRawBeta + 256;
 // One stage per chunk in flight: the operands the state MMAs read.
 constexpr int kWLbo = 144;                        // [-Kbar; Qbar]: core matrices adjacent along K are
 constexpr int kWSbo = 32 * kWLbo;                 //   144 B apart, so a warp's row stores hit all banks
@@ -73,23 +74,23 @@ constexpr int kStW = 0;                           // tf32 [64 tok][128 dk], K-ma
 constexpr int kStKt = kStW + 8 * kWSbo;           // tf32 [128 dk][32 tok]: Kr, then Kt in place
 constexpr int kStBo = kStKt + 16384;              // tf32 [32 tok][32 tok]: Bo = Mqk T'
 constexpr int kStDec = kStBo + 4096;              // fp32 [128]: 2^G_last
+constexpr int kStOst = kStW;                      // bf16 [32][136]: output staging, once the
+                                                  //   projection has read [-Kbar; Qbar]
 constexpr int kStageBytes = kStDec + 512;
 constexpr int kPair = kStage0 + 2 * kStageBytes;  // 3 x [48][136] bf16
 constexpr int kPairQ = kPair;
 constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
 constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
 constexpr int kPairEnd = kPairKR + 48 * kRowB * 2;
-// Group B's work space (the diagonal inverse blocks form while group A refills the pairs).
+// Group B's work space.
 constexpr int kAtHi = kPairEnd;                   // tf32 [32][32] core matrices: T'^T
 constexpr int kTinv = kAtHi + 4096;               // fp32 [32][36]: (I + Diag(beta) A)^-1
 constexpr int kPscr = kTinv + 32 * kSq * 4;       // fp32 [16][16]: N21 T11 (and 2 x [8][8] before)
-// Handed from group A to group B, one copy per chunk parity.
-constexpr int kNt = kPscr + 1024;                 // fp32 [2][32][36]: (Diag(beta) A)^T
-constexpr int kMq = kNt + 2 * 32 * kSq * 4;       // fp32 [2][32][36]: Mqk
-constexpr int kBetaS = kMq + 2 * 32 * kSq * 4;    // fp32 [2][32]: beta of the chunk
-constexpr int kQuart = kBetaS + 256;              // fp32 [4][128]: per-quarter decay products
-constexpr int kOst = kQuart + 4 * 128 * 4;        // bf16 [32][136]: output staging
-constexpr int kBars = kOst + 32 * kRowB * 2;
+constexpr int kNt = kPscr + 1024;                 // fp32 [32][36]: (Diag(beta) A)^T
+constexpr int kMq = kNt + 32 * kSq * 4;           // fp32 [32][36]: Mqk
+constexpr int kBetaS = kMq + 32 * kSq * 4;        // fp32 [32]: beta of the chunk
+constexpr int kQuart = kBetaS + 128;              // fp32 [4][128]: per-quarter decay products
+constexpr int kBars = kQuart + 4 * 128 * 4;
 constexpr int kSmemTc = kBars + 128;
 static_assert(kStage0 % 128 == 0 && kStageBytes % 128 == 0 && kAtHi % 128 == 0, "operand alignment");
 static_assert(kSmemTc <= 227 * 1024, "one CTA per SM");
@@ -113,7 +114,8 @@ struct Bars {
     uint64_t oread[2];   // D1 buffer b read out by the state warps (count kStateThreads)
     uint64_t kt;         // group B's Kt MMA complete (tcgen05.commit)
     uint64_t ab_full[2]; // group A -> B: chunk operands of parity p ready (count kProdThreads)
-    uint64_t ab_empty[2];// group B -> A: Mqk, N, beta of parity p consumed (count kSolveThreads)
+    uint64_t ab_empty;   // group B -> A: the pair operands and raw v, beta of a chunk consumed
+                         //   (count kSolveThreads, one phase per chunk)
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -197,12 +199,25 @@ __device__ __forceinline__ void st_pair(uint8_t *base, int elem, float lo, float
     *reinterpret_cast<uint32_t *>(base + 2 * elem) = pack_bf16(lo, hi);
 }
 
-// Producer-side raw loads of one chunk: q, k, a rows (unpadded) or v rows (padded) + beta.
-__device__ __forceinline__ void load_qka(const PrefillArgs &a, uint8_t *smem, int t0, int L, int h, int ptid) {
-    const __nv_bfloat16 *src[3] = {a.q, a.k, a.g_raw};
+// Raw loads of one chunk (cp.async, zero-filled past the sequence end): the gate tile into
+// buffer `buf`, the q and k tiles, and the (padded) v tile with beta into buffer `buf`.
+__device__ __forceinline__ void load_a(const PrefillArgs &a, uint8_t *smem, int t0, int L, int h, int ptid, int buf) {
 #pragma unroll
-    for (int m = 0; m < 6; ++m) {
-        const int idx = ptid + kProdThreads * m;  // 0 .. 1535
+    for (int m = 0; m < 2; ++m) {
+        const int idx = ptid + kProdThreads * m;  // 0 .. 511
+        const int row = idx >> 4, vec = idx & 15;
+        const bool valid = row < L;
+        const size_t tok = (size_t)(t0 + (valid ? row : 0));
+        cp_async_16(smem_addr(smem + kRawA + buf * 8192 + row * 256 + vec * 16),
+                    a.g_raw + (tok * a.num_heads + h) * kHeadDim + vec * 8, valid ? 16u : 0u);
+    }
+}
+
+__device__ __forceinline__ void load_qk(const PrefillArgs &a, uint8_t *smem, int t0, int L, int h, int ptid) {
+    const __nv_bfloat16 *src[2] = {a.q, a.k};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int idx = ptid + kProdThreads * m;  // 0 .. 1023
         const int tensor = idx >> 9;
         const int row = (idx >> 4) & 31;
         const int vec = idx & 15;
@@ -213,20 +228,20 @@ __device__ __forceinline__ void load_qka(const PrefillArgs &a, uint8_t *smem, in
     }
 }
 
-__device__ __forceinline__ void load_vb(const PrefillArgs &a, uint8_t *smem, int t0, int L, int h, int ptid) {
+__device__ __forceinline__ void load_vb(const PrefillArgs &a, uint8_t *smem, int t0, int L, int h, int ptid, int buf) {
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
         const int idx = ptid + kProdThreads * m;  // 0 .. 511
         const int row = idx >> 4, vec = idx & 15;
         const bool valid = row < L;
         const size_t tok = (size_t)(t0 + (valid ? row : 0));
-        cp_async_16(smem_addr(smem + kRawV + (row * kRowB + vec * 8) * 2),
+        cp_async_16(smem_addr(smem + kRawV + buf * kRawVBytes + (row * kRowB + vec * 8) * 2),
                     a.v + (tok * a.num_heads + h) * kHeadDim + vec * 8, valid ? 16u : 0u);
     }
     if (ptid < 32) {
         const bool valid = ptid < L;
         const size_t tok = (size_t)(t0 + (valid ? ptid : 0));
-        cp_async_4(smem_addr(smem + kRawBeta + ptid * 4), a.beta + tok * a.num_heads + h, valid ? 4u : 0u);
+        cp_async_4(smem_addr(smem + kRawBeta + buf * 128 + ptid * 4), a.beta + tok * a.num_heads + h, valid ? 4u : 0u);
     }
 }
 
@@ -248,30 +263,66 @@ __device__ __forceinline__ void kt_to_stage(uint32_t tmem, uint8_t *stage, int b
     }
 }
 
-// V^T of the chunk into its D1 buffer (lane = dv, column = token); the output pass also
-// zeroes the 32 columns the projection accumulates Qbar S into.
+// V^T of the chunk into its D1 buffer (lane = dv, column = token), by group B: its warp b
+// owns lane quadrant b. The output pass also zeroes the 32 columns the projection
+// accumulates Qbar S into.
 template <bool kPass1>
-__device__ __forceinline__ void v_to_tmem(uint32_t tmem, const uint8_t *rv, int db, int warp, int lane) {
-    if (kPass1 && warp >= 4) return;
-    const int quad = warp & 3;
+__device__ __forceinline__ void v_to_tmem(uint32_t tmem, const uint8_t *rv, int db, int bwarp, int lane) {
+    const int dv = 32 * bwarp + lane;
     float v0[16], v1[16];
-    if (warp < 4) {
-        const int dv = 32 * quad + lane;
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            v0[t] = bfv(rv, t * kRowB + dv);
-            v1[t] = bfv(rv, (16 + t) * kRowB + dv);
-        }
-    } else {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) v0[t] = v1[t] = 0.0f;
+    for (int t = 0; t < 16; ++t) {
+        v0[t] = bfv(rv, t * kRowB + dv);
+        v1[t] = bfv(rv, (16 + t) * kRowB + dv);
     }
     // output pass: D1 = [V | 0] (64 columns per buffer); window pass: D1 = V (32)
-    const uint32_t col = kPass1 ? kColD1 + 32 * db : kColD1 + 64 * db + 32 * (warp >> 2);
-    const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16) + col;
+    const uint32_t taddr = tmem + ((uint32_t)(32 * bwarp) << 16) + (kPass1 ? kColD1 + 32 * db : kColD1 + 64 * db);
     tmem_st16(taddr, v0);
     tmem_st16(taddr + 16, v1);
+    if (!kPass1) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) v0[t] = 0.0f;
+        tmem_st16(taddr + 32, v0);
+        tmem_st16(taddr + 48, v0);
+    }
     tmem_wait_st();
+}
+
+// One 16 x 16 block of the pair products by one warp (mma.sync m16n8k16, BF16, FP32
+// accumulate): `which` 0 is Mqk (query rows), 1 is N = Diag(beta) A (key rows); block 0 and 1
+// are the diagonal blocks of the two halves, 2 the off-diagonal one. Mqk is stored row-major
+// with the causal mask, N transposed and strictly lower.
+__device__ __forceinline__ void pair_block(const uint8_t *smem, int which, int blk, int lane, const float *rb,
+                                           float *mq_s, float *nt_s) {
+    const int g = lane >> 2, t4 = lane & 3;
+    const uint8_t *Lb = smem + (which ? kPairKL : kPairQ);
+    const uint8_t *Rb = smem + kPairKR;
+    const int row0 = 16 * blk;
+    float acc[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        uint32_t af[4], bfr[4];
+        ldsm_x4(af, smem_addr(Lb + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
+        ldsm_x4(bfr, smem_addr(Rb + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
+                                     ((lane >> 3) & 1) * 8) * 2));
+        mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
+        mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
+    }
+    const int oi = (blk == 0) ? 0 : 16;
+    const int oj = (blk == 1) ? 16 : 0;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = oi + g + 8 * (e >> 1);
+            const int j = oj + 8 * nt + 2 * t4 + (e & 1);
+            const float val = acc[nt][e];
+            if (which == 0)
+                mq_s[i * kSq + j] = (j <= i) ? val : 0.0f;
+            else
+                nt_s[j * kSq + i] = (j < i) ? val * rb[i] : 0.0f;
+        }
+    }
 }
 
 // (I + N_d)^-1 of the 16 x 16 diagonal block at (o, o) of a strictly lower triangular N
@@ -339,41 +390,42 @@ __device__ __forceinline__ void invert_diag16(const float *nt, float *inv, float
 }
 
 // Group A, per chunk: the gate and decay factors, the chunk operands of the state MMAs
-// (stage), V^T into the chunk's D1 buffer, the raw loads of the next chunk, and the pair
-// products Mqk and Diag(beta) A for group B.
+// (stage) and of the pair products, and the raw loads of the next chunk.
 template <bool kPass1>
 __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int n, int h, int bos,
                               int eos, int nchunks) {
+    (void)tmem;
     const int ptid = threadIdx.x;  // 0 .. 255
-    const int warp = ptid >> 5, lane = ptid & 31;
-    const int g = lane >> 2, t4 = lane & 3;
     uint8_t *const pairQ = smem + kPairQ;
     uint8_t *const pairKL = smem + kPairKL;
     uint8_t *const pairKR = smem + kPairKR;
     float *const quart_s = reinterpret_cast<float *>(smem + kQuart);
     const uint8_t *const rq = smem + kRawQ;
     const uint8_t *const rk = smem + kRawK;
-    const uint8_t *const ra = smem + kRawA;
-    const uint8_t *const rv = smem + kRawV;
-    const float *const rb = reinterpret_cast<const float *>(smem + kRawBeta);
-
+    // cp.async groups, in commit order: a(0), a(1), [q, k, v, beta](0); then per chunk c: a(c + 2)
+    // once the gate of c has read its buffer, [q, k, v, beta](c + 1) once the operands of c are
+    // written (groups past the end are empty)
+    auto rows_of = [&](int cc) { return min(kChunk, eos - (bos + kChunk * cc)); };
+    if (nchunks > 0) load_a(a, smem, bos, rows_of(0), h, ptid, 0);
+    cp_async_commit();
+    if (nchunks > 1) load_a(a, smem, bos + kChunk, rows_of(1), h, ptid, 1);
+    cp_async_commit();
     if (nchunks > 0) {
-        const int L0 = min(kChunk, eos - bos);
-        load_qka(a, smem, bos, L0, h, ptid);
-        load_vb(a, smem, bos, L0, h, ptid);
+        load_qk(a, smem, bos, rows_of(0), h, ptid);
+        load_vb(a, smem, bos, rows_of(0), h, ptid, 0);
     }
     cp_async_commit();
 
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = bos + kChunk * c;
         const int L = min(kChunk, eos - t0);
-        const int ps = c & 1, db = c & 1;
+        const int ps = c & 1;
         uint8_t *const stage = smem + kStage0 + ps * kStageBytes;
-        float *const nt_s = reinterpret_cast<float *>(smem + kNt) + ps * 32 * kSq;
-        float *const mq_s = reinterpret_cast<float *>(smem + kMq) + ps * 32 * kSq;
-        float *const beta_s = reinterpret_cast<float *>(smem + kBetaS) + ps * 32;
-        cp_async_wait<0>();
-        bar_named(kBarProd, kProdThreads);
+        const uint8_t *const ra = smem + kRawA + ps * 8192;
+        if (c == 0) {  // later gate tiles were waited for a chunk earlier
+            cp_async_wait<2>();
+            bar_named(kBarProd, kProdThreads);
+        }
 
         // ---- 1. decays, anchored factors, chunk operands. Thread = (channel pair, 8-token
         //      quarter). With d the per-token decay, every factor is a running product of d or
@@ -421,12 +473,18 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             const float R0 = rcp(P0[7]), R1 = rcp(P1[7]);
             *reinterpret_cast<float2 *>(quart_s + qt * 128 + ch) = make_float2(P0[7], P1[7]);
             {  // the gate needs no shared state; before the stores: stage ps is free once the
-               // state update of chunk c - 2 has read it, the hand-off buffers of parity ps once
-               // group B is through with chunk c - 2
+               // state update and the output staging of chunk c - 2 are done with it, the pair
+               // operands (and the raw v, beta buffer the next load refills) once group B is
+               // through with chunk c - 1
                 bool lost = c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status);
-                lost = lost || (c >= 2 && !wait_or_abort(&B->ab_empty[ps], ((c >> 1) + 1) & 1, B, a.status));
+                lost = lost || (c >= 2 && !wait_or_abort(&B->oread[ps], ((c >> 1) + 1) & 1, B, a.status));
+                lost = lost || (c >= 1 && !wait_or_abort(&B->ab_empty, (c - 1) & 1, B, a.status));
+                cp_async_wait<0>();  // q, k, v, beta of chunk c and the gate tile of chunk c + 1
                 if (bar_any(kBarProd, kProdThreads, lost)) break;
             }
+            // this chunk's gate tile is consumed: its buffer takes chunk c + 2
+            if (c + 2 < nchunks) load_a(a, smem, t0 + 2 * kChunk, rows_of(c + 2), h, ptid, ps);
+            cp_async_commit();
             float2 T[4];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) T[q4] = *reinterpret_cast<const float2 *>(quart_s + q4 * 128 + ch);
@@ -495,72 +553,24 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 *reinterpret_cast<float2 *>(stage + kStDec + 4 * ch) =
                     make_float2(T[0].x * T[1].x * T[2].x * T[3].x, T[0].y * T[1].y * T[2].y * T[3].y);
         }
-        // ---- 1b. V^T of chunk c into its D1 buffer and beta aside, so the raw buffers can
-        //      refill with chunk c + 1.
-        {
-            const bool lost = c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status);
-            if (bar_any(kBarProd, kProdThreads, lost)) break;
-        }
-        tc_fence_after();
-        v_to_tmem<kPass1>(tmem, rv, db, warp, lane);
-        if (ptid < kChunk) beta_s[ptid] = rb[ptid];
+        // the operands of chunk c go to group B; the raw q, k tiles refill with chunk c + 1, and
+        // v, beta with chunk c + 1 in the other buffer
+        fence_async_smem();
         bar_named(kBarProd, kProdThreads);
         if (c + 1 < nchunks) {
-            const int t1 = t0 + kChunk;
-            load_qka(a, smem, t1, min(kChunk, eos - t1), h, ptid);
-            load_vb(a, smem, t1, min(kChunk, eos - t1), h, ptid);
+            load_qk(a, smem, t0 + kChunk, rows_of(c + 1), h, ptid);
+            load_vb(a, smem, t0 + kChunk, rows_of(c + 1), h, ptid, ps ^ 1);
         }
         cp_async_commit();
-
-        // ---- 2. Mqk (causal) and N^T = (Diag(beta) A)^T: three 16x16 blocks each (warps 0-5)
-        if (warp < 6) {
-          if (!(kPass1 && warp < 3)) {  // the Mqk blocks are not needed by the window pass
-            const int which = warp / 3;
-            const int blk = warp % 3;
-            const uint8_t *Lb = which ? pairKL : pairQ;
-            const int row0 = 16 * blk;
-            float acc[2][4] = {};
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t af[4], bfr[4];
-                ldsm_x4(af, smem_addr(Lb + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
-                ldsm_x4(bfr, smem_addr(pairKR + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
-                                                  ((lane >> 3) & 1) * 8) * 2));
-                mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
-                mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
-            }
-            const int oi = (blk == 0) ? 0 : 16;
-            const int oj = (blk == 1) ? 16 : 0;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = oi + g + 8 * (e >> 1);
-                    const int j = oj + 8 * nt + 2 * t4 + (e & 1);
-                    const float val = acc[nt][e];
-                    if (which == 0) {
-                        mq_s[i * kSq + j] = (j <= i) ? val : 0.0f;
-                    } else {
-                        nt_s[j * kSq + i] = (j < i) ? val * beta_s[i] : 0.0f;
-                    }
-                }
-            }
-          }
-        } else if (!kPass1) {
-            for (int idx = ptid - 192; idx < 256; idx += 64)
-                mq_s[(idx >> 4) * kSq + 16 + (idx & 15)] = 0.0f;  // upper-right block of Mqk
-        }
-        // the stage operands, D1 and the pair products of chunk c go to group B
-        fence_async_smem();
-        tc_fence_before();
         mbar_arrive(&B->ab_full[ps]);
     }
     cp_async_wait<0>();
 }
 
-// Group B, per chunk: (I + Diag(beta) A)^-1 by 16 x 16 blocks, T' in TF32, the Kt MMA and
-// Bo = Mqk T' (mma.sync TF32) while it runs, then the hand-off: Kt read back into the stage
-// in place of Kr, and the stage released to the state warps.
+// Group B, per chunk: the pair products Mqk and Diag(beta) A (mma.sync), V^T into the chunk's
+// D1 buffer, (I + Diag(beta) A)^-1 by 16 x 16 blocks, T' in TF32, the Kt MMA and Bo = Mqk T'
+// (mma.sync TF32) while it runs, then the hand-off: Kt read back into the stage in place of
+// Kr, and the stage released to the state warps.
 template <bool kPass1>
 __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int nchunks) {
     const int btid = threadIdx.x - kFirstSolveWarp * 32;  // 0 .. 127
@@ -571,27 +581,46 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
     float *const pscr = reinterpret_cast<float *>(smem + kPscr);
     uint8_t *const at_hi = smem + kAtHi;
 
+    float *const nt_s = reinterpret_cast<float *>(smem + kNt);
+    float *const mq_s = reinterpret_cast<float *>(smem + kMq);
+    float *const beta_s = reinterpret_cast<float *>(smem + kBetaS);
+
     for (int c = 0; c < nchunks; ++c) {
-        const int ps = c & 1;
+        const int ps = c & 1, db = c & 1;
         uint8_t *const stage = smem + kStage0 + ps * kStageBytes;
-        const float *const nt_s = reinterpret_cast<const float *>(smem + kNt) + ps * 32 * kSq;
-        const float *const mq_s = reinterpret_cast<const float *>(smem + kMq) + ps * 32 * kSq;
-        const float *const beta_s = reinterpret_cast<const float *>(smem + kBetaS) + ps * 32;
-        {
-            const bool lost = !wait_or_abort(&B->ab_full[ps], (c >> 1) & 1, B, a.status);
+        const uint8_t *const rv = smem + kRawV + ps * kRawVBytes;
+        const float *const rb = reinterpret_cast<const float *>(smem + kRawBeta) + ps * 32;
+        {  // chunk c's operands are ready; its D1 buffer is free once chunk c - 2 is read out
+            bool lost = !wait_or_abort(&B->ab_full[ps], (c >> 1) & 1, B, a.status);
+            lost = lost || (c >= 2 && !wait_or_abort(&B->oread[db], ((c >> 1) + 1) & 1, B, a.status));
             if (bar_any(kBarSolve, kSolveThreads, lost)) break;
         }
         tc_fence_after();
+        // ---- pair products: warp w takes N block w (the diagonal ones are inverted at once by
+        //      the same warp) and then Mqk block w; warp 3 zeroes the blocks above the diagonal.
+        //      Then V^T into D1 and beta aside, after which group A may refill what was read.
+        if (bwarp < 3) {
+            pair_block(smem, 1, bwarp, lane, rb, mq_s, nt_s);
+            if (bwarp < 2) {
+                __syncwarp();
+                invert_diag16(nt_s, tinv, pscr + 64 * bwarp, 16 * bwarp, lane);
+            }
+            if (!kPass1) pair_block(smem, 0, bwarp, lane, rb, mq_s, nt_s);
+        } else {
+            for (int idx = lane; idx < 256; idx += 32) {
+                const int i = idx >> 4, j = 16 + (idx & 15);
+                if (!kPass1) mq_s[i * kSq + j] = 0.0f;
+                tinv[i * kSq + j] = 0.0f;
+            }
+        }
+        v_to_tmem<kPass1>(tmem, rv, db, bwarp, lane);
+        if (btid < kChunk) beta_s[btid] = rb[btid];
+        tc_fence_before();
+        bar_named(kBarSolve, kSolveThreads);
+        mbar_arrive(&B->ab_empty);
 
         // ---- T = (I + N)^-1, N = Diag(beta) A strictly lower triangular, in FP32 by 16 x 16
-        //      blocks: the diagonal blocks (warps 0, 1), then T21 = -T22 N21 T11.
-        if (bwarp < 2) {
-            invert_diag16(nt_s, tinv, pscr + 64 * bwarp, 16 * bwarp, lane);
-        } else {
-            for (int idx = btid - 64; idx < 256; idx += 64)
-                tinv[(idx >> 4) * kSq + 16 + (idx & 15)] = 0.0f;  // upper-right block
-        }
-        bar_named(kBarSolve, kSolveThreads);
+        //      blocks: the diagonal blocks are inverted above, then T21 = -T22 N21 T11.
         {
             const int i = btid >> 3, j2 = 2 * (btid & 7);
             float p0 = 0.0f, p1 = 0.0f;
@@ -675,7 +704,6 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                     make_float2(tf32f(acc[2]), tf32f(acc[3]));
             }
         }
-        mbar_arrive(&B->ab_empty[ps]);
         // ---- hand-off: Kt in place of Kr, then the stage goes to the state warps
         {
             const bool lost = kt_thread && !wait_or_abort(&B->kt, c & 1, B, a.status);
@@ -749,7 +777,6 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
     const int dv = 32 * quad + lane;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const bool mma_thread = (warp == kFirstStateWarp) && (lane == 0);
-    uint8_t *const ost = smem + kOst;
 
     // initial state -> S^T buffer 0 (lane = dv, column = dk)
 #pragma unroll 1
@@ -821,8 +848,8 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         tmem_ld16(tmem + lane_base + kColD1 + 64 * db + 32, o0);
         tmem_ld16(tmem + lane_base + kColD1 + 64 * db + 48, o1);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&B->oread[db]);
+        // staged in this chunk's [-Kbar; Qbar] operand, which the projection has read
+        uint8_t *const ost = const_cast<uint8_t *>(stage) + kStOst;
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
             st_bf16(ost, t * kRowB + dv, o0[t]);
@@ -840,6 +867,9 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                 *reinterpret_cast<uint4 *>(a.out + ((size_t)(t0 + row) * a.num_heads + h) * kHeadDim + vec * 8) = v4;
             }
         }
+        // D1 buffer db and the staging area are free again
+        tc_fence_before();
+        mbar_arrive(&B->oread[db]);
         alive = !bar_any(kBarState, kStateThreads, B->abort != 0);
     }
 
@@ -1019,8 +1049,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         mbar_init(&B->prep[1], kSolveThreads);
         mbar_init(&B->ab_full[0], kProdThreads);
         mbar_init(&B->ab_full[1], kProdThreads);
-        mbar_init(&B->ab_empty[0], kSolveThreads);
-        mbar_init(&B->ab_empty[1], kSolveThreads);
+        mbar_init(&B->ab_empty, kSolveThreads);
         mbar_init(&B->g1, 1);
         mbar_init(&B->go, 1);
         mbar_init(&B->kt, 1);
