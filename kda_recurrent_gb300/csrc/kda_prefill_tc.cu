@@ -181,12 +181,12 @@ __device__ __forceinline__ float rcp(float x) {
     return y;
 }
 
-// Per-token decay d = exp(g) of one channel from the raw gate a.
-__device__ __forceinline__ float gate_decay(float av, int mode, float lower_bound) {
-    if (mode == KDA_GATE_LOWER_BOUND)  // exp(lb sigmoid(a))
-        return ex2(lower_bound * kLog2e * rcp(1.0f + ex2(-av * kLog2e)));
-    if (mode == KDA_GATE_SOFTPLUS)  // exp(-softplus(a)) = 1 / (1 + e^a)
-        return rcp(1.0f + ex2(av * kLog2e));
+// Per-token decay d = exp(g) of one channel from the raw gate a, for a gate mode fixed at
+// compile time (lb2 = lower_bound * log2 e).
+template <int kMode>
+__device__ __forceinline__ float gate_decay_m(float av, float lb2) {
+    if (kMode == KDA_GATE_LOWER_BOUND) return ex2(lb2 * rcp(1.0f + ex2(-av * kLog2e)));  // exp(lb sigmoid(a))
+    if (kMode == KDA_GATE_SOFTPLUS) return rcp(1.0f + ex2(av * kLog2e));               // exp(-softplus(a))
     return ex2(av * kLog2e);
 }
 
@@ -435,17 +435,28 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             const int cp = ptid & 63, qt = ptid >> 6;
             const int ch = 2 * cp;
             float d0[8], d1[8];
+            // the gate mode is uniform, so each mode gets its own loop
+            auto decays = [&](auto mode) {
+                constexpr int kMode = decltype(mode)::value;
+                const float lb2 = a.lower_bound * kLog2e;
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
-                const int i = 8 * qt + ii;
-                d0[ii] = d1[ii] = 1.0f;
-                if (i < L) {
-                    float a0, a1;
-                    unpack_bf16x2(*reinterpret_cast<const uint32_t *>(ra + 2 * (i * 128 + ch)), a0, a1);
-                    d0[ii] = gate_decay(a0, a.gate_mode, a.lower_bound);
-                    d1[ii] = gate_decay(a1, a.gate_mode, a.lower_bound);
+                for (int ii = 0; ii < 8; ++ii) {
+                    const int i = 8 * qt + ii;
+                    d0[ii] = d1[ii] = 1.0f;
+                    if (i < L) {
+                        float a0, a1;
+                        unpack_bf16x2(*reinterpret_cast<const uint32_t *>(ra + 2 * (i * 128 + ch)), a0, a1);
+                        d0[ii] = gate_decay_m<kMode>(a0, lb2);
+                        d1[ii] = gate_decay_m<kMode>(a1, lb2);
+                    }
                 }
-            }
+            };
+            if (a.gate_mode == KDA_GATE_LOWER_BOUND)
+                decays(std::integral_constant<int, KDA_GATE_LOWER_BOUND>{});
+            else if (a.gate_mode == KDA_GATE_SOFTPLUS)
+                decays(std::integral_constant<int, KDA_GATE_SOFTPLUS>{});
+            else
+                decays(std::integral_constant<int, KDA_GATE_LOG_DECAY>{});
             // P: inclusive prefix of d; S: exclusive suffix of d. The anchored factor F is made
             // of 1/d: the exclusive suffix of 1/d before the anchor (quarters 0 and 2), which
             // is P / P_7, and the inclusive prefix of 1/d from the anchor on (quarters 1 and
