@@ -255,8 +255,12 @@ struct StreamShape {
     static constexpr uint32_t kTokBytes = 4 * kHeadDim * 2;  // q, k, g_raw, v rows of one token
     static constexpr int VEC = StateVec<T>::kElems;
     static constexpr int RPP = kDecodeThreads / (kHeadDim / VEC);
+    // BF16 states are updated by two groups of four warps, one item each (see below)
+    static constexpr bool kGroups = sizeof(T) == 2;
+    static constexpr int kGroupBytes = 2 * 8 * kHeadDim * 4 + 4 * kHeadDim * 4 + kMaxTokensPerRow * 4;
     static constexpr int kRed = 2 * RPP * kHeadDim * 4;
-    static constexpr int kFixed = kRed + 4 * kHeadDim * 4 + kMaxTokensPerRow * 4 + 2 * kMaxStages * 8;
+    static constexpr int kFixed = (kGroups ? 2 * kGroupBytes : kRed + 4 * kHeadDim * 4 + kMaxTokensPerRow * 4) +
+                                  2 * kMaxStages * 8;
     static constexpr int kStreamSmem = 220 * 1024;
     static __host__ __device__ uint32_t stage_bytes(int tokens) { return kItemBytes + kTokBytes * tokens; }
     static __host__ __device__ int stages(int tokens) {
@@ -267,6 +271,137 @@ struct StreamShape {
 };
 
 __device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kDecodeThreads) : "memory"); }
+
+// BF16 states, streaming schedule: the eight compute warps form two groups of four, and
+// group g updates the items with an even (g = 0) or odd (g = 1) local index, so one group's
+// barriers and latencies overlap the other's arithmetic. The state stays in its ring stage:
+// thread (row group rg, 8-column block cb) reads its 16 x 8 slice once to form the decayed
+// projections S^T k and S^T q, and once more to write Diag(exp g) S + k u^T back in place.
+__device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t *stages, uint8_t *scratch, int NS,
+                                                 uint32_t stage_bytes, uint64_t *full, uint64_t *done, int64_t first,
+                                                 int64_t stride, int mine) {
+    using SS = StreamShape<__nv_bfloat16>;
+    const int tid = threadIdx.x;
+    const int grp = tid >> 7, gt = tid & 127;
+    const int cb = gt & 15, rg = gt >> 4;  // columns 8 cb .. 8 cb + 7, rows 16 rg .. 16 rg + 15
+    float *const s_red = reinterpret_cast<float *>(scratch + grp * SS::kGroupBytes);  // [2][8][128]
+    float *const s_k = s_red + 2 * 8 * kHeadDim;
+    float *const s_q = s_k + kHeadDim;
+    float *const s_decay = s_q + kHeadDim;
+    float *const s_u = s_decay + kHeadDim;
+    float *const s_beta = s_u + kHeadDim;  // [kMaxTokensPerRow]
+    const int TT = a.tokens;
+    const int H = a.num_heads;
+    auto gbar = [&]() {
+        if (grp == 0)
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+        else
+            asm volatile("bar.sync 3, 128;" ::: "memory");
+    };
+    auto slot_of = [&](int64_t item) -> int64_t {
+        const int32_t slot = __ldg(a.slot_idx + (int)(item / H));
+        return (slot >= 0 && (int64_t)slot < a.num_slots) ? (int64_t)slot : -1;
+    };
+    auto tok_index = [&](int64_t item, int t) -> size_t {
+        const int64_t r = item / H, h = item % H;
+        return ((size_t)r * TT + t) * (size_t)H + (size_t)h;
+    };
+    int64_t slot_next = grp < mine ? slot_of(first + grp * stride) : -1;
+    float beta_next = (grp < mine && gt < TT) ? a.beta[tok_index(first + grp * stride, gt)] : 0.0f;
+    for (int kk = grp; kk < mine; kk += 2) {
+        const int st = kk % NS;
+        const int64_t item = first + (int64_t)kk * stride;
+        const int r = (int)(item / H);
+        const int64_t slot = slot_next;
+        const float beta_mine = beta_next;
+        if (kk + 2 < mine) {
+            slot_next = slot_of(item + 2 * stride);
+            if (gt < TT) beta_next = a.beta[tok_index(item + 2 * stride, gt)];
+        }
+        if (!mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u)) {
+            report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+            break;
+        }
+        if (slot < 0) {
+            for (int t = 0; t < TT; ++t) a.out[tok_index(item, t) * kHeadDim + gt] = __float2bfloat16_rn(0.0f);
+            const int32_t raw_slot = __ldg(a.slot_idx + r);
+            if (gt == 0 && (int64_t)raw_slot >= a.num_slots && item % H == 0)
+                report_error(a.status, KDA_ERR_DEVICE_INPUT, r);
+            mbar_arrive(&done[st]);
+            continue;
+        }
+        uint8_t *const S = stages + (size_t)st * stage_bytes;  // bf16 [128 dk][128 dv]
+        for (int t = 0; t < TT; ++t) {
+            const __nv_bfloat16 *trow =
+                reinterpret_cast<const __nv_bfloat16 *>(S + SS::kItemBytes + t * SS::kTokBytes);
+            gbar();  // the previous step's use of the group's vectors (and state slice) is over
+            {
+                const float av = __bfloat162float(trow[2 * kHeadDim + gt]);
+                s_decay[gt] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
+                s_k[gt] = __bfloat162float(trow[kHeadDim + gt]);
+                s_q[gt] = __bfloat162float(trow[gt]);
+            }
+            if (t == 0 && gt < TT) s_beta[gt] = beta_mine;
+            gbar();
+            const TokenScalars ts = token_scalars(s_q, s_k, a);
+            float wk[8], wq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wk[e] = wq[e] = 0.0f;
+#pragma unroll 4
+            for (int i = 0; i < 16; ++i) {
+                const int row = 16 * rg + i;
+                float x[8];
+                StateVec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(S + (row * kHeadDim + 8 * cb) * 2), x);
+                const float d = s_decay[row], kr = s_k[row], qr = s_q[row];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float y = x[e] * d;
+                    wk[e] = fmaf(y, kr, wk[e]);
+                    wq[e] = fmaf(y, qr, wq[e]);
+                }
+            }
+            float *const rk = s_red + rg * kHeadDim + 8 * cb;
+            float *const rq = s_red + (8 + rg) * kHeadDim + 8 * cb;
+            *reinterpret_cast<float4 *>(rk) = make_float4(wk[0] * ts.rk, wk[1] * ts.rk, wk[2] * ts.rk, wk[3] * ts.rk);
+            *reinterpret_cast<float4 *>(rk + 4) = make_float4(wk[4] * ts.rk, wk[5] * ts.rk, wk[6] * ts.rk, wk[7] * ts.rk);
+            *reinterpret_cast<float4 *>(rq) = make_float4(wq[0] * ts.rq, wq[1] * ts.rq, wq[2] * ts.rq, wq[3] * ts.rq);
+            *reinterpret_cast<float4 *>(rq + 4) = make_float4(wq[4] * ts.rq, wq[5] * ts.rq, wq[6] * ts.rq, wq[7] * ts.rq);
+            gbar();
+            {  // column j = gt
+                float w_k = 0.0f, w_q = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    w_k += s_red[i * kHeadDim + gt];
+                    w_q += s_red[(8 + i) * kHeadDim + gt];
+                }
+                const float u = beta_of(s_beta[t], a) * (__bfloat162float(trow[3 * kHeadDim + gt]) - w_k);
+                s_u[gt] = u;
+                a.out[tok_index(item, t) * kHeadDim + gt] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
+            }
+            gbar();
+            float uv[8];
+            {
+                const float4 u0 = *reinterpret_cast<const float4 *>(s_u + 8 * cb);
+                const float4 u1 = *reinterpret_cast<const float4 *>(s_u + 8 * cb + 4);
+                uv[0] = u0.x, uv[1] = u0.y, uv[2] = u0.z, uv[3] = u0.w;
+                uv[4] = u1.x, uv[5] = u1.y, uv[6] = u1.z, uv[7] = u1.w;
+            }
+#pragma unroll 4
+            for (int i = 0; i < 16; ++i) {
+                const int row = 16 * rg + i;
+                uint4 *const p = reinterpret_cast<uint4 *>(S + (row * kHeadDim + 8 * cb) * 2);
+                float x[8];
+                StateVec<__nv_bfloat16>::unpack(*p, x);
+                const float d = s_decay[row], kr = s_k[row] * ts.rk;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = fmaf(kr, uv[e], x[e] * d);
+                *p = StateVec<__nv_bfloat16>::pack(x);
+            }
+        }
+        fence_async_smem();
+        mbar_arrive(&done[st]);
+    }
+}
 
 // One CTA per SM: warps 0-7 update states; warp 8 (lane 0) moves them. Stage s is filled by
 // bulk copies that complete `full[s]`; the compute warps arrive on `done[s]` once the
@@ -293,7 +428,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     float *const s_decay = s_q + kHeadDim;
     float *const s_u = s_decay + kHeadDim;
     float *const s_beta = s_u + kHeadDim;  // [kMaxTokensPerRow]
-    uint64_t *const full = reinterpret_cast<uint64_t *>(s_beta + kMaxTokensPerRow);
+    uint64_t *const full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes + SS::kFixed - 2 * SS::kMaxStages * 8);
     uint64_t *const done = full + SS::kMaxStages;
 
     const int tid = threadIdx.x;
@@ -304,7 +439,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     if (tid == 0) {
         for (int st = 0; st < NS; ++st) {
             mbar_init(&full[st], 1);
-            mbar_init(&done[st], kDecodeThreads);
+            mbar_init(&done[st], SS::kGroups ? kDecodeThreads / 2 : kDecodeThreads);
         }
         fence_mbar_init();
     }
@@ -377,6 +512,10 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     }
 
     // ---- compute warps
+    if constexpr (SS::kGroups) {
+        stream_groups_bf16(a, stages, smem + NS * stage_bytes, NS, stage_bytes, full, done, first, stride, mine);
+        return;
+    }
     const int cg = tid % VPR, rg = tid / VPR;
     int64_t slot_next = mine > 0 ? slot_of(first) : -1;
     float beta_next = (mine > 0 && tid < TT) ? a.beta[tok_index(first, tid)] : 0.0f;
