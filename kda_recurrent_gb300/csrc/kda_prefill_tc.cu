@@ -58,6 +58,13 @@ constexpr int kKtThread = (kFirstSolveWarp + 1) * 32;  // group B thread that is
 constexpr int kRowB = 136;  // padded bf16 row stride (ldmatrix operands)
 constexpr int kSq = 36;     // fp32 32 x 32 tiles
 constexpr float kLog2e = 1.4426950408889634f;
+// Operands the tcgen05 MMAs read from shared memory are stored as plain FP32: kind::tf32
+// reads only the TF32 bits and drops the 13 low mantissa bits, i.e. truncates toward zero.
+// For mantissas spread log-uniformly the mean relative loss of that truncation is
+// 2^-11 / ln 2 ~ 0.72 * 2^-11, so values pre-scaled by this factor (folded into a factor
+// that is multiplied in anyway) reach the tensor core without bias, and with the same error
+// spread as rounding to nearest. It replaces an explicit rounding per element.
+constexpr float kTruncBias = 1.0f + 0.75f / 2048.0f;
 
 // ---- shared-memory map (bytes)
 constexpr int kRawQ = 0;                          // bf16 [32][128]
@@ -167,8 +174,6 @@ __device__ __forceinline__ int w_off(int row, int col) {
     return (row >> 3) * kWSbo + (col >> 2) * kWLbo + (row & 7) * 16 + (col & 3) * 4;
 }
 
-__device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
-
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -247,7 +252,8 @@ __device__ __forceinline__ void load_vb(const PrefillArgs &a, uint8_t *smem, int
 
 // ------------------------------------------------------------------ producers
 
-// Kt^T (TMEM lane = dk, column = token) -> the stage's Kt operand (tf32, [dk][token]), by
+// Kt^T (TMEM lane = dk, column = token) -> the stage's Kt operand ([dk][token], read as TF32
+// by the state update, which truncates it; T' carries the factor that offsets that), by
 // group B: its warp b owns lane quadrant b.
 __device__ __forceinline__ void kt_to_stage(uint32_t tmem, uint8_t *stage, int bwarp, int lane) {
     const int dk = 32 * bwarp + lane;
@@ -259,7 +265,7 @@ __device__ __forceinline__ void kt_to_stage(uint32_t tmem, uint8_t *stage, int b
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4)
             *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(dk, 16 * half + 4 * e4, 1024)) =
-                make_float4(tf32f(v[4 * e4]), tf32f(v[4 * e4 + 1]), tf32f(v[4 * e4 + 2]), tf32f(v[4 * e4 + 3]));
+                make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
     }
 }
 
@@ -510,6 +516,9 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     post1 *= T[q4].y;
                 }
             }
+            // the stage operands are truncated to TF32 by the MMAs that read them
+            const float preT0 = pre0 * kTruncBias, preT1 = pre1 * kTruncBias;
+            const float postT0 = post0 * kTruncBias, postT1 = post1 * kTruncBias;
             // off-diagonal factors 2^(G_i - G_15) (i >= 16) and 2^(G_15 - G_j) (j < 16)
             const float od0 = (qt == 0) ? T[1].x : ((qt == 3) ? T[2].x : 1.0f);
             const float od1 = (qt == 0) ? T[1].y : ((qt == 3) ? T[2].y : 1.0f);
@@ -543,14 +552,12 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                     const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
                     st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
                 }
-                const float fb0 = pre0 * P0[ii], fb1 = pre1 * P1[ii];  // 2^G_i
-                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) =
-                    make_float2(tf32f(-k0 * fb0), tf32f(-k1 * fb1));
+                const float fb0 = preT0 * P0[ii], fb1 = preT1 * P1[ii];  // 2^G_i
+                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) = make_float2(-k0 * fb0, -k1 * fb1);
                 if (!kPass1)
-                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) =
-                        make_float2(tf32f(q0 * fb0), tf32f(q1 * fb1));
-                kr0[ii] = tf32f(k0 * (S0[ii] * post0));  // 2^(G_L - G_i)
-                kr1[ii] = tf32f(k1 * (S1[ii] * post1));
+                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) = make_float2(q0 * fb0, q1 * fb1);
+                kr0[ii] = k0 * (S0[ii] * postT0);  // 2^(G_L - G_i)
+                kr1[ii] = k1 * (S1[ii] * postT1);
             }
 #pragma unroll
             for (int h4 = 0; h4 < 2; ++h4) {
@@ -659,16 +666,18 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         }
         bar_named(kBarSolve, kSolveThreads);
 
-        // ---- T' = T Diag(beta), stored as T'^T (row j, K index i) in TF32
+        // ---- T' = T Diag(beta), stored as T'^T (row j, K index i) for the TF32 Kt MMA
         {
             const int j = btid & 31;
-            const float bj = beta_s[j];
+            // T' is truncated by the Kt MMA and Kt = Kr^T T' again by the state update: the
+            // factor twice leaves both without bias
+            const float bj = beta_s[j] * (kTruncBias * kTruncBias);
 #pragma unroll
             for (int qh = 0; qh < 2; ++qh) {
                 const int q = (btid >> 5) + 4 * qh;  // T'[4q .. 4q + 3][j]
                 float hi[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) hi[r] = tf32f(tinv[(4 * q + r) * kSq + j] * bj);
+                for (int r = 0; r < 4; ++r) hi[r] = tinv[(4 * q + r) * kSq + j] * bj;
                 const int off = core_off_tf32(j, 4 * q, 1024);
                 *reinterpret_cast<float4 *>(at_hi + off) = make_float4(hi[0], hi[1], hi[2], hi[3]);
             }
@@ -704,15 +713,15 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                     const uint32_t af[4] = {to_tf32(mq_s[r0 * kSq + k0]), to_tf32(mq_s[(r0 + 8) * kSq + k0]),
                                             to_tf32(mq_s[r0 * kSq + k0 + 4]), to_tf32(mq_s[(r0 + 8) * kSq + k0 + 4])};
                     const int jn = 8 * nt + g;
-                    const float bj = beta_s[jn];
+                    const float bj = beta_s[jn] * kTruncBias;  // Bo is truncated by the output MMA
                     mma_tf32_1688(acc, af, to_tf32(tinv[k0 * kSq + jn] * bj),
                                   to_tf32(tinv[(k0 + 4) * kSq + jn] * bj));
                 }
                 const int i0 = 16 * mt + g, j0 = 8 * nt + 2 * t4;
                 *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0, j0, 1024)) =
-                    make_float2(tf32f(acc[0]), tf32f(acc[1]));
+                    make_float2(acc[0], acc[1]);
                 *reinterpret_cast<float2 *>(stage + kStBo + core_off_tf32(i0 + 8, j0, 1024)) =
-                    make_float2(tf32f(acc[2]), tf32f(acc[3]));
+                    make_float2(acc[2], acc[3]);
             }
         }
         // ---- hand-off: Kt in place of Kr, then the stage goes to the state warps
