@@ -19,13 +19,17 @@
 // memory, TF32), issued by the producers off the serial chain. The state is ping-ponged between two TMEM buffers so that
 // the decay runs while the projection reads the previous buffer.
 //
-// Warp roles (one CTA per (sequence, head) chain, 12 warps):
-//   warps 0-7  producers: raw loads (cp.async), gate and decay products, pair products
-//              Mqk and Diag(beta) A (mma.sync), (I + Diag(beta) A)^-1 in FP32 by 16 x 16 blocks
-//              (forward substitution on the diagonal blocks, one product pair for the
-//              off-diagonal block), Bo (mma.sync, TF32), Kt (tcgen05), V^T into TMEM;
-//   warps 8-11 state warps (one per TMEM lane quadrant): initial/final state, the decay,
-//              the output read-out and store; lane 0 of warp 8 issues the state MMAs.
+// Warp roles (one CTA per (sequence, head) chain, 16 warps), a chunk per group in flight:
+//   warps 0-7   group A: raw loads (cp.async), gate and decay products, the pair operands
+//               (bf16) and the stage operands ([-Kbar; Qbar], Kr, 2^G_last), in packed FP32
+//               arithmetic on the two channels a thread owns;
+//   warps 8-11  group B: pair products Mqk and Diag(beta) A (mma.sync), V^T into TMEM,
+//               (I + Diag(beta) A)^-1 in FP32 by 16 x 16 blocks, T', the Kt MMA (tcgen05),
+//               Bo (mma.sync, TF32) and the hand-off of the stage;
+//   warps 12-15 state warps (one per TMEM lane quadrant): initial/final state, the decay,
+//               the output read-out and store; lane 0 of warp 12 issues the state MMAs.
+// Two stages of operands are in flight; the pair operands, the raw v and beta buffers and
+// TMEM's D1 buffers are each released as soon as their reader is done with them.
 // Exponent range: per 16-token half, factors are anchored at the half's 8th token, built
 // as running products of the per-token decays and their inverses (no per-element exp of a
 // prefix); the off-diagonal block factors through the half boundary (both factors <= 1).
@@ -73,18 +77,15 @@ constexpr int kRawA = kRawK + 8192;               // bf16 [2][32][128]: the gate
 constexpr int kRawV = kRawA + 2 * 8192;           // bf16 [2][32][136]: v, one buffer per chunk parity
 constexpr int kRawVBytes = 32 * kRowB * 2;
 constexpr int kRawBeta = kRawV + 2 * kRawVBytes;  // fp32 [2][32]: beta, one buffer per chunk parity
-constexpr int kStage0 = kRawBeta + 256;
+constexpr int kStage0 = (kRawBeta + 256 + 1023) / 1024 * 1024;  // 1024-aligned (swizzle atoms)
 // One stage per chunk in flight: the operands the state MMAs read.
-constexpr int kWLbo = 144;                        // [-Kbar; Qbar]: core matrices adjacent along K are
-constexpr int kWSbo = 32 * kWLbo;                 //   144 B apart, so a warp's row stores hit all banks
-constexpr int kStW = 0;                           // tf32 [64 tok][128 dk], K-major core matrices
-constexpr int kStKt = kStW + 8 * kWSbo;           // tf32 [128 dk][32 tok]: Kr, then Kt in place
+constexpr int kStW = 0;                           // tf32 [4 K-atoms][64 tok][32 dk], 128-byte swizzle
+constexpr int kStKt = kStW + 4 * 8192;            // tf32 [128 dk][32 tok]: Kr, then Kt in place
 constexpr int kStBo = kStKt + 16384;              // tf32 [32 tok][32 tok]: Bo = Mqk T'
 constexpr int kStDec = kStBo + 4096;              // fp32 [128]: 2^G_last
-constexpr int kStOst = kStW;                      // bf16 [32][136]: output staging, once the
-                                                  //   projection has read [-Kbar; Qbar]
-constexpr int kStageBytes = kStDec + 512;
-constexpr int kPair = kStage0 + 2 * kStageBytes;  // 3 x [48][136] bf16
+constexpr int kStageBytes = (kStDec + 512 + 1023) / 1024 * 1024;
+constexpr int kOst = kStage0 + 2 * kStageBytes;   // bf16 [32][136]: output staging
+constexpr int kPair = kOst + 32 * kRowB * 2;      // 3 x [48][136] bf16
 constexpr int kPairQ = kPair;
 constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
 constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
@@ -100,7 +101,8 @@ constexpr int kQuart = kBetaS + 128;              // fp32 [4][128]: per-quarter 
 constexpr int kBars = kQuart + 4 * 128 * 4;
 constexpr int kSmemTc = kBars + 128;
 static_assert(kStage0 % 128 == 0 && kStageBytes % 128 == 0 && kAtHi % 128 == 0, "operand alignment");
-static_assert(kSmemTc <= 227 * 1024, "one CTA per SM");
+constexpr int kSmemLaunch = kSmemTc + 1024;  // plus the alignment slack
+static_assert(kSmemLaunch <= 227 * 1024, "one CTA per SM");
 
 // ---- tensor-memory map (columns; 512 allocated)
 constexpr uint32_t kTmemCols = 512;
@@ -118,11 +120,13 @@ struct Bars {
     uint64_t go;         // output MMA complete (tcgen05.commit)
     uint64_t g2;         // state update MMA complete (tcgen05.commit)
     uint64_t g2s[2];     // state update of a chunk on stage s complete (tcgen05.commit)
-    uint64_t oread[2];   // D1 buffer b read out by the state warps (count kStateThreads)
+    uint64_t oread[2];   // D1 buffer b read out by the state warps (count kStateThreads); in the
+                         //   window pass also the stage of that parity consumed
     uint64_t kt;         // group B's Kt MMA complete (tcgen05.commit)
     uint64_t ab_full[2]; // group A -> B: chunk operands of parity p ready (count kProdThreads)
-    uint64_t ab_empty;   // group B -> A: the pair operands and raw v, beta of a chunk consumed
+    uint64_t ab_empty;   // group B -> A: the pair operands of a chunk consumed
                          //   (count kSolveThreads, one phase per chunk)
+    uint64_t vfree;      // group B -> A: the raw v, beta of a chunk consumed (same counting)
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -169,10 +173,14 @@ __device__ __forceinline__ int core_off_tf32(int row, int col, int sbo) {
     return (row >> 3) * sbo + (col >> 2) * 128 + (row & 7) * 16 + (col & 3) * 4;
 }
 
-// Byte offset of element (token, dk) of the [-Kbar; Qbar] operand (K-major, padded K stride).
+// Byte offset of element (token, dk) of the [-Kbar; Qbar] operand: K-major with the 128-byte
+// swizzle, one 8 KiB atom per 32 dk (64 rows of 128 bytes); the 16-byte chunk of a row is
+// XORed with the row's index within its 8-row group, so a warp's row stores hit all banks.
 __device__ __forceinline__ int w_off(int row, int col) {
-    return (row >> 3) * kWSbo + (col >> 2) * kWLbo + (row & 7) * 16 + (col & 3) * 4;
+    return (col >> 5) * 8192 + (row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 2) & 7) ^ (row & 7)) << 4) +
+           (col & 3) * 4;
 }
+
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -200,8 +208,40 @@ __device__ __forceinline__ void unpack_bf16x2(uint32_t w, float &lo, float &hi) 
     hi = __uint_as_float(w & 0xffff0000u);
 }
 
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Packed FP32 arithmetic on the two channels a producer thread owns (one instruction for both
+// lanes of the pair, each rounded to nearest as the scalar operation is).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+
+// gate_decay_m for both channels of a pair
+template <int kMode>
+__device__ __forceinline__ float2 gate_decay2(float2 av, float lb2) {
+    if (kMode == KDA_GATE_LOWER_BOUND) {
+        const float2 e = mul2(av, splat2(-kLog2e));
+        const float2 den = add2(make_float2(ex2(e.x), ex2(e.y)), splat2(1.0f));
+        const float2 x = mul2(make_float2(rcp(den.x), rcp(den.y)), splat2(lb2));
+        return make_float2(ex2(x.x), ex2(x.y));
+    }
+    const float2 e = mul2(av, splat2(kLog2e));
+    if (kMode == KDA_GATE_SOFTPLUS) {
+        const float2 den = add2(make_float2(ex2(e.x), ex2(e.y)), splat2(1.0f));
+        return make_float2(rcp(den.x), rcp(den.y));
+    }
+    return make_float2(ex2(e.x), ex2(e.y));
+}
+
 __device__ __forceinline__ void st_pair(uint8_t *base, int elem, float lo, float hi) {
     *reinterpret_cast<uint32_t *>(base + 2 * elem) = pack_bf16(lo, hi);
+}
+
+__device__ __forceinline__ void st_pair(uint8_t *base, int elem, float2 v) {
+    *reinterpret_cast<uint32_t *>(base + 2 * elem) = pack_bf16(v.x, v.y);
 }
 
 // Raw loads of one chunk (cp.async, zero-filled past the sequence end): the gate tile into
@@ -371,13 +411,10 @@ __device__ __forceinline__ void invert_diag16(const float *nt, float *inv, float
         nl[l] = nt[(o + l) * kSq + r0 + i];
         tl[l] = *reinterpret_cast<const float2 *>(inv + (o + l) * kSq + o + j2);
     }
-    float p0 = 0.0f, p1 = 0.0f;
+    float2 p = splat2(0.0f);
 #pragma unroll
-    for (int l = 0; l < 8; ++l) {
-        p0 = fmaf(nl[l], tl[l].x, p0);
-        p1 = fmaf(nl[l], tl[l].y, p1);
-    }
-    *reinterpret_cast<float2 *>(scr + i * 8 + j2) = make_float2(p0, p1);
+    for (int l = 0; l < 8; ++l) p = fma2(splat2(nl[l]), tl[l], p);
+    *reinterpret_cast<float2 *>(scr + i * 8 + j2) = p;
     __syncwarp();
     float tr[8];
     float2 pl[8];
@@ -386,13 +423,10 @@ __device__ __forceinline__ void invert_diag16(const float *nt, float *inv, float
         tr[k] = inv[(r0 + i) * kSq + r0 + k];
         pl[k] = *reinterpret_cast<const float2 *>(scr + k * 8 + j2);
     }
-    float q0 = 0.0f, q1 = 0.0f;
+    float2 q = splat2(0.0f);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        q0 = fmaf(tr[k], pl[k].x, q0);
-        q1 = fmaf(tr[k], pl[k].y, q1);
-    }
-    *reinterpret_cast<float2 *>(inv + (r0 + i) * kSq + o + j2) = make_float2(-q0, -q1);
+    for (int k = 0; k < 8; ++k) q = fma2(splat2(-tr[k]), pl[k], q);
+    *reinterpret_cast<float2 *>(inv + (r0 + i) * kSq + o + j2) = q;
 }
 
 // Group A, per chunk: the gate and decay factors, the chunk operands of the state MMAs
@@ -422,6 +456,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
     }
     cp_async_commit();
 
+    bool vlost = false;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = bos + kChunk * c;
         const int L = min(kChunk, eos - t0);
@@ -440,7 +475,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         {
             const int cp = ptid & 63, qt = ptid >> 6;
             const int ch = 2 * cp;
-            float d0[8], d1[8];
+            float2 d[8];  // per-token decays of channels ch, ch + 1
             // the gate mode is uniform, so each mode gets its own loop
             auto decays = [&](auto mode) {
                 constexpr int kMode = decltype(mode)::value;
@@ -448,13 +483,10 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
 #pragma unroll
                 for (int ii = 0; ii < 8; ++ii) {
                     const int i = 8 * qt + ii;
-                    d0[ii] = d1[ii] = 1.0f;
-                    if (i < L) {
-                        float a0, a1;
-                        unpack_bf16x2(*reinterpret_cast<const uint32_t *>(ra + 2 * (i * 128 + ch)), a0, a1);
-                        d0[ii] = gate_decay_m<kMode>(a0, lb2);
-                        d1[ii] = gate_decay_m<kMode>(a1, lb2);
-                    }
+                    d[ii] = splat2(1.0f);
+                    if (i < L)
+                        d[ii] = gate_decay2<kMode>(
+                            unpack_bf16x2(*reinterpret_cast<const uint32_t *>(ra + 2 * (i * 128 + ch))), lb2);
                 }
             };
             if (a.gate_mode == KDA_GATE_LOWER_BOUND)
@@ -468,33 +500,27 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             // is P / P_7, and the inclusive prefix of 1/d from the anchor on (quarters 1 and
             // 3), which is S / P_7, so one reciprocal per channel serves the quarter.
             const bool before_anchor = (qt & 1) == 0;
-            float P0[8], P1[8], S0[8], S1[8];
+            float2 P[8], S[8];
             {
-                float r0 = 1.0f, r1 = 1.0f;
+                float2 r = splat2(1.0f);
 #pragma unroll
                 for (int ii = 0; ii < 8; ++ii) {
-                    r0 *= d0[ii];
-                    r1 *= d1[ii];
-                    P0[ii] = r0;
-                    P1[ii] = r1;
+                    r = mul2(r, d[ii]);
+                    P[ii] = r;
                 }
-                r0 = r1 = 1.0f;
+                r = splat2(1.0f);
 #pragma unroll
                 for (int ii = 7; ii >= 0; --ii) {
-                    S0[ii] = r0;
-                    S1[ii] = r1;
-                    r0 *= d0[ii];
-                    r1 *= d1[ii];
+                    S[ii] = r;
+                    r = mul2(r, d[ii]);
                 }
             }
-            const float R0 = rcp(P0[7]), R1 = rcp(P1[7]);
-            *reinterpret_cast<float2 *>(quart_s + qt * 128 + ch) = make_float2(P0[7], P1[7]);
+            const float2 R = make_float2(rcp(P[7].x), rcp(P[7].y));
+            *reinterpret_cast<float2 *>(quart_s + qt * 128 + ch) = P[7];
             {  // the gate needs no shared state; before the stores: stage ps is free once the
-               // state update and the output staging of chunk c - 2 are done with it, the pair
-               // operands (and the raw v, beta buffer the next load refills) once group B is
-               // through with chunk c - 1
-                bool lost = c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status);
-                lost = lost || (c >= 2 && !wait_or_abort(&B->oread[ps], ((c >> 1) + 1) & 1, B, a.status));
+               // state update of chunk c - 2 is done with it, the pair operands once group B has
+               // read those of chunk c - 1
+                bool lost = vlost || (c >= 2 && !wait_or_abort(&B->g2s[ps], ((c >> 1) + 1) & 1, B, a.status));
                 lost = lost || (c >= 1 && !wait_or_abort(&B->ab_empty, (c - 1) & 1, B, a.status));
                 cp_async_wait<0>();  // q, k, v, beta of chunk c and the gate tile of chunk c + 1
                 if (bar_any(kBarProd, kProdThreads, lost)) break;
@@ -505,77 +531,66 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             float2 T[4];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) T[q4] = *reinterpret_cast<const float2 *>(quart_s + q4 * 128 + ch);
-            float pre0 = 1.0f, pre1 = 1.0f, post0 = 1.0f, post1 = 1.0f;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                if (q4 < qt) {
-                    pre0 *= T[q4].x;
-                    pre1 *= T[q4].y;
-                } else if (q4 > qt) {
-                    post0 *= T[q4].x;
-                    post1 *= T[q4].y;
-                }
-            }
+            const float2 one = splat2(1.0f);
+            // whole-quarter products before (pre) and after (post) this quarter
+            const float2 pre = mul2(mul2(qt > 0 ? T[0] : one, qt > 1 ? T[1] : one), qt > 2 ? T[2] : one);
+            const float2 post = mul2(mul2(qt < 1 ? T[1] : one, qt < 2 ? T[2] : one), qt < 3 ? T[3] : one);
             // the stage operands are truncated to TF32 by the MMAs that read them
-            const float preT0 = pre0 * kTruncBias, preT1 = pre1 * kTruncBias;
-            const float postT0 = post0 * kTruncBias, postT1 = post1 * kTruncBias;
+            const float2 preT = mul2(pre, splat2(kTruncBias)), npreT = mul2(pre, splat2(-kTruncBias));
+            const float2 postT = mul2(post, splat2(kTruncBias));
             // off-diagonal factors 2^(G_i - G_15) (i >= 16) and 2^(G_15 - G_j) (j < 16)
-            const float od0 = (qt == 0) ? T[1].x : ((qt == 3) ? T[2].x : 1.0f);
-            const float od1 = (qt == 0) ? T[1].y : ((qt == 3) ? T[2].y : 1.0f);
+            const float2 od = (qt == 0) ? T[1] : ((qt == 3) ? T[2] : one);
             // the largest factors of the quarter: P_7 and 1/P_7 bound P, S and F when d <= 1,
             // and F at its far end is checked directly for other gates
-            const float fmax0 = before_anchor ? P0[0] * R0 : R0, fmax1 = before_anchor ? P1[0] * R1 : R1;
-            if (!(fmax0 < 3.0e38f && fmax1 < 3.0e38f && R0 < 3.0e38f && R1 < 3.0e38f && P0[7] < 3.0e38f &&
-                  P1[7] < 3.0e38f))
+            const float fmax0 = before_anchor ? P[0].x * R.x : R.x, fmax1 = before_anchor ? P[0].y * R.y : R.y;
+            if (!(fmax0 < 3.0e38f && fmax1 < 3.0e38f && R.x < 3.0e38f && R.y < 3.0e38f && P[7].x < 3.0e38f &&
+                  P[7].y < 3.0e38f))
                 report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
-            float kr0[8], kr1[8];
-            // left factor fl (query / key rows of the diagonal blocks) and right factor fr
-            // (key columns): F and S before the anchor, P and F from it on
+            // left factor fl = P Rl (query / key rows of the diagonal blocks) and right factor
+            // fr = S Rr (key columns): F and S before the anchor, P and F from it on
+            const float2 Rl = before_anchor ? R : one, Rr = before_anchor ? one : R;
+            const float2 sc = splat2(a.scale);
+            float2 kr[8];
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 const int i = 8 * qt + ii;
-                float k0, k1, q0, q1;
-                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rk + 2 * (i * 128 + ch)), k0, k1);
-                unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rq + 2 * (i * 128 + ch)), q0, q1);
-                q0 *= a.scale;
-                q1 *= a.scale;
-                const float fl0 = before_anchor ? P0[ii] * R0 : P0[ii], fl1 = before_anchor ? P1[ii] * R1 : P1[ii];
-                const float fr0 = before_anchor ? S0[ii] : S0[ii] * R0, fr1 = before_anchor ? S1[ii] : S1[ii] * R1;
-                if (!kPass1) st_pair(pairQ, i * kRowB + ch, q0 * fl0, q1 * fl1);
-                st_pair(pairKL, i * kRowB + ch, k0 * fl0, k1 * fl1);
-                st_pair(pairKR, i * kRowB + ch, k0 * fr0, k1 * fr1);
+                const float2 k2 = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rk + 2 * (i * 128 + ch)));
+                const float2 q2 = mul2(unpack_bf16x2(*reinterpret_cast<const uint32_t *>(rq + 2 * (i * 128 + ch))), sc);
+                const float2 fl = mul2(P[ii], Rl), fr = mul2(S[ii], Rr);
+                if (!kPass1) st_pair(pairQ, i * kRowB + ch, mul2(q2, fl));
+                st_pair(pairKL, i * kRowB + ch, mul2(k2, fl));
+                st_pair(pairKR, i * kRowB + ch, mul2(k2, fr));
                 if (qt >= 2) {
-                    const float fo0 = od0 * P0[ii], fo1 = od1 * P1[ii];
-                    if (!kPass1) st_pair(pairQ, (16 + i) * kRowB + ch, q0 * fo0, q1 * fo1);
-                    st_pair(pairKL, (16 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                    const float2 fo = mul2(od, P[ii]);
+                    if (!kPass1) st_pair(pairQ, (16 + i) * kRowB + ch, mul2(q2, fo));
+                    st_pair(pairKL, (16 + i) * kRowB + ch, mul2(k2, fo));
                 } else {
-                    const float fo0 = S0[ii] * od0, fo1 = S1[ii] * od1;
-                    st_pair(pairKR, (32 + i) * kRowB + ch, k0 * fo0, k1 * fo1);
+                    st_pair(pairKR, (32 + i) * kRowB + ch, mul2(k2, mul2(S[ii], od)));
                 }
-                const float fb0 = preT0 * P0[ii], fb1 = preT1 * P1[ii];  // 2^G_i
-                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) = make_float2(-k0 * fb0, -k1 * fb1);
+                // 2^G_i and 2^(G_L - G_i)
+                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) = mul2(k2, mul2(npreT, P[ii]));
                 if (!kPass1)
-                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) = make_float2(q0 * fb0, q1 * fb1);
-                kr0[ii] = k0 * (S0[ii] * postT0);  // 2^(G_L - G_i)
-                kr1[ii] = k1 * (S1[ii] * postT1);
+                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) = mul2(q2, mul2(preT, P[ii]));
+                kr[ii] = mul2(k2, mul2(S[ii], postT));
             }
 #pragma unroll
             for (int h4 = 0; h4 < 2; ++h4) {
                 const int i0 = 8 * qt + 4 * h4;
                 *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch, i0, 1024)) =
-                    make_float4(kr0[4 * h4], kr0[4 * h4 + 1], kr0[4 * h4 + 2], kr0[4 * h4 + 3]);
+                    make_float4(kr[4 * h4].x, kr[4 * h4 + 1].x, kr[4 * h4 + 2].x, kr[4 * h4 + 3].x);
                 *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch + 1, i0, 1024)) =
-                    make_float4(kr1[4 * h4], kr1[4 * h4 + 1], kr1[4 * h4 + 2], kr1[4 * h4 + 3]);
+                    make_float4(kr[4 * h4].y, kr[4 * h4 + 1].y, kr[4 * h4 + 2].y, kr[4 * h4 + 3].y);
             }
             if (qt == 0)
-                *reinterpret_cast<float2 *>(stage + kStDec + 4 * ch) =
-                    make_float2(T[0].x * T[1].x * T[2].x * T[3].x, T[0].y * T[1].y * T[2].y * T[3].y);
+                *reinterpret_cast<float2 *>(stage + kStDec + 4 * ch) = mul2(mul2(T[0], T[1]), mul2(T[2], T[3]));
         }
         // the operands of chunk c go to group B; the raw q, k tiles refill with chunk c + 1, and
         // v, beta with chunk c + 1 in the other buffer
         fence_async_smem();
         bar_named(kBarProd, kProdThreads);
-        if (c + 1 < nchunks) {
+        // the raw v, beta buffer of chunk c - 1 is free once group B has moved them out
+        vlost = c >= 1 && !wait_or_abort(&B->vfree, (c - 1) & 1, B, a.status);
+        if (c + 1 < nchunks && !vlost) {
             load_qk(a, smem, t0 + kChunk, rows_of(c + 1), h, ptid);
             load_vb(a, smem, t0 + kChunk, rows_of(c + 1), h, ptid, ps ^ 1);
         }
@@ -619,12 +634,13 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         //      Then V^T into D1 and beta aside, after which group A may refill what was read.
         if (bwarp < 3) {
             pair_block(smem, 1, bwarp, lane, rb, mq_s, nt_s);
-            if (bwarp < 2) {
-                __syncwarp();
-                invert_diag16(nt_s, tinv, pscr + 64 * bwarp, 16 * bwarp, lane);
-            }
             if (!kPass1) pair_block(smem, 0, bwarp, lane, rb, mq_s, nt_s);
-        } else {
+        }
+        mbar_arrive(&B->ab_empty);  // this thread's reads of the pair operands are done
+        if (bwarp < 2) {
+            __syncwarp();
+            invert_diag16(nt_s, tinv, pscr + 64 * bwarp, 16 * bwarp, lane);
+        } else if (bwarp == 3) {
             for (int idx = lane; idx < 256; idx += 32) {
                 const int i = idx >> 4, j = 16 + (idx & 15);
                 if (!kPass1) mq_s[i * kSq + j] = 0.0f;
@@ -635,34 +651,26 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         if (btid < kChunk) beta_s[btid] = rb[btid];
         tc_fence_before();
         bar_named(kBarSolve, kSolveThreads);
-        mbar_arrive(&B->ab_empty);
+        mbar_arrive(&B->vfree);
 
         // ---- T = (I + N)^-1, N = Diag(beta) A strictly lower triangular, in FP32 by 16 x 16
         //      blocks: the diagonal blocks are inverted above, then T21 = -T22 N21 T11.
         {
             const int i = btid >> 3, j2 = 2 * (btid & 7);
-            float p0 = 0.0f, p1 = 0.0f;
+            float2 p = splat2(0.0f);
 #pragma unroll
-            for (int l = 0; l < 16; ++l) {
-                const float nv = nt_s[l * kSq + 16 + i];
-                const float2 tv = *reinterpret_cast<const float2 *>(tinv + l * kSq + j2);
-                p0 = fmaf(nv, tv.x, p0);
-                p1 = fmaf(nv, tv.y, p1);
-            }
-            *reinterpret_cast<float2 *>(pscr + i * 16 + j2) = make_float2(p0, p1);
+            for (int l = 0; l < 16; ++l)
+                p = fma2(splat2(nt_s[l * kSq + 16 + i]), *reinterpret_cast<const float2 *>(tinv + l * kSq + j2), p);
+            *reinterpret_cast<float2 *>(pscr + i * 16 + j2) = p;
         }
         bar_named(kBarSolve, kSolveThreads);
         {
             const int i = btid >> 3, j2 = 2 * (btid & 7);
-            float p0 = 0.0f, p1 = 0.0f;
+            float2 p = splat2(0.0f);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float tv = tinv[(16 + i) * kSq + 16 + k];
-                const float2 pv = *reinterpret_cast<const float2 *>(pscr + k * 16 + j2);
-                p0 = fmaf(tv, pv.x, p0);
-                p1 = fmaf(tv, pv.y, p1);
-            }
-            *reinterpret_cast<float2 *>(tinv + (16 + i) * kSq + j2) = make_float2(-p0, -p1);
+            for (int k = 0; k < 16; ++k)
+                p = fma2(splat2(-tinv[(16 + i) * kSq + 16 + k]), *reinterpret_cast<const float2 *>(pscr + k * 16 + j2), p);
+            *reinterpret_cast<float2 *>(tinv + (16 + i) * kSq + j2) = p;
         }
         bar_named(kBarSolve, kSolveThreads);
 
@@ -776,14 +784,20 @@ __device__ __forceinline__ void decay_columns(uint32_t src, uint32_t dst, const 
         if (j + 1 < blocks) tmem_ld32(src + 32 * (j + 1), v[1]);
         const float *d0 = dec + ((32 * j) & 127);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[0][e] *= d0[e];
+        for (int e = 0; e < 32; e += 2) {
+            const float2 x = mul2(make_float2(v[0][e], v[0][e + 1]), *reinterpret_cast<const float2 *>(d0 + e));
+            v[0][e] = x.x, v[0][e + 1] = x.y;
+        }
         tmem_st32(dst + 32 * j, v[0]);
         if (j + 1 >= blocks) break;
         tmem_wait_ld();
         if (j + 2 < blocks) tmem_ld32(src + 32 * (j + 2), v[0]);
         const float *d1 = dec + ((32 * (j + 1)) & 127);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[1][e] *= d1[e];
+        for (int e = 0; e < 32; e += 2) {
+            const float2 x = mul2(make_float2(v[1][e], v[1][e + 1]), *reinterpret_cast<const float2 *>(d1 + e));
+            v[1][e] = x.x, v[1][e + 1] = x.y;
+        }
         tmem_st32(dst + 32 * (j + 1), v[1]);
     }
     tmem_wait_st();
@@ -825,7 +839,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
 #pragma unroll
             for (int s = 0; s < 16; ++s)
                 mma_tf32_ts(tmem + kColD1 + 64 * db, tmem + cur + 8 * s,
-                            smem_desc_kmajor(wbase + 2 * kWLbo * s, kWLbo, kWSbo), kIdescG1, true);
+                            smem_desc_sw128(wbase + (s >> 2) * 8192 + (s & 3) * 32), kIdescG1, true);
             mma_commit(&B->g1);
         }
         __syncwarp();
@@ -868,8 +882,12 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         tmem_ld16(tmem + lane_base + kColD1 + 64 * db + 32, o0);
         tmem_ld16(tmem + lane_base + kColD1 + 64 * db + 48, o1);
         tmem_wait_ld();
-        // staged in this chunk's [-Kbar; Qbar] operand, which the projection has read
-        uint8_t *const ost = const_cast<uint8_t *>(stage) + kStOst;
+        // D1 buffer db is free again
+        tc_fence_before();
+        mbar_arrive(&B->oread[db]);
+        // staged through shared memory for 16-byte row stores; the buffer is reused by the
+        // next chunk only after the barrier that closes this iteration
+        uint8_t *const ost = smem + kOst;
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
             st_bf16(ost, t * kRowB + dv, o0[t]);
@@ -887,9 +905,6 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                 *reinterpret_cast<uint4 *>(a.out + ((size_t)(t0 + row) * a.num_heads + h) * kHeadDim + vec * 8) = v4;
             }
         }
-        // D1 buffer db and the staging area are free again
-        tc_fence_before();
-        mbar_arrive(&B->oread[db]);
         alive = !bar_any(kBarState, kStateThreads, B->abort != 0);
     }
 
@@ -961,7 +976,7 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
             const uint32_t wbase = smem_addr(stage + kStW);
 #pragma unroll
             for (int s = 0; s < 16; ++s) {
-                const uint64_t bd = smem_desc_kmajor(wbase + 2 * kWLbo * s, kWLbo, kWSbo);
+                const uint64_t bd = smem_desc_sw128(wbase + (s >> 2) * 8192 + (s & 3) * 32);
                 mma_tf32_ts(tmem + kColD1 + 32 * db, tmem + kColS + 8 * s, bd, kIdescN32, true);
                 mma_tf32_ts(tmem + kColD1M + 32 * db, tmem + kColM + 8 * s, bd, kIdescN32, s > 0);
             }
@@ -1049,7 +1064,9 @@ __device__ __forceinline__ float *window_slot(const PrefillArgs &a, int chain, i
 
 template <bool kPass1>
 __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the swizzled operands need 1024-byte alignment; the launch reserves the slack
+    uint8_t *const smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     Bars *B = reinterpret_cast<Bars *>(smem + kBars);
     const int warp = threadIdx.x >> 5;
     const int H = a.num_heads;
@@ -1070,6 +1087,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         mbar_init(&B->ab_full[0], kProdThreads);
         mbar_init(&B->ab_full[1], kProdThreads);
         mbar_init(&B->ab_empty, kSolveThreads);
+        mbar_init(&B->vfree, kSolveThreads);
         mbar_init(&B->g1, 1);
         mbar_init(&B->go, 1);
         mbar_init(&B->kt, 1);
@@ -1201,7 +1219,7 @@ cudaError_t configure_once() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kda_prefill_tc_kernel<kPass1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+        e = cudaFuncSetAttribute(kda_prefill_tc_kernel<kPass1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
@@ -1237,14 +1255,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     if (W > 1) {
         e = configure_once<true>();
         if (e != cudaSuccess) return e;
-        kda_prefill_tc_kernel<true><<<(unsigned)(chains * W), kThreadsTc, kSmemTc, stream>>>(a);
+        kda_prefill_tc_kernel<true><<<(unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, 0, stream>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    kda_prefill_tc_kernel<false><<<(unsigned)(chains * W), kThreadsTc, kSmemTc, stream>>>(a);
+    kda_prefill_tc_kernel<false><<<(unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -112,6 +112,21 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lb
     return d;
 }
 
+// Shared-memory descriptor, K-major layout with the 128-byte swizzle: rows of 128 bytes in
+// 8-row groups of 1024 bytes (the stride byte offset), the 16-byte chunk index of a row
+// XORed with the row's index within its group. The group must start 1024-byte aligned; the
+// start address may step through a row in 32-byte K steps. The leading byte offset is not
+// used by this layout.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for the sm_100 family
+    d |= (uint64_t)2 << 61;  // layout type: 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor for kind::tf32 / kind::f16 with FP32 accumulation, both
 // operands K-major, dense. `ab_format`: 1 = BF16 (kind::f16), 2 = TF32 (kind::tf32).
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_format, uint32_t M, uint32_t N) {
