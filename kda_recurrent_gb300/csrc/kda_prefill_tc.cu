@@ -587,6 +587,7 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         // the operands of chunk c go to group B; the raw q, k tiles refill with chunk c + 1, and
         // v, beta with chunk c + 1 in the other buffer
         fence_async_smem();
+        mbar_arrive(&B->ab_full[ps]);
         bar_named(kBarProd, kProdThreads);
         // the raw v, beta buffer of chunk c - 1 is free once group B has moved them out
         vlost = c >= 1 && !wait_or_abort(&B->vfree, (c - 1) & 1, B, a.status);
@@ -595,7 +596,6 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
             load_vb(a, smem, t0 + kChunk, rows_of(c + 1), h, ptid, ps ^ 1);
         }
         cp_async_commit();
-        mbar_arrive(&B->ab_full[ps]);
     }
     cp_async_wait<0>();
 }
