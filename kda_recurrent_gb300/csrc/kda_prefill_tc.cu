@@ -586,11 +586,13 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
         }
         // the operands of chunk c go to group B; the raw q, k tiles refill with chunk c + 1, and
         // v, beta with chunk c + 1 in the other buffer
+        // the raw v, beta buffer of chunk c - 1 is free once group B has moved them out; the
+        // wait comes before this chunk's hand-off so that group B cannot complete the phase of
+        // chunk c before it is observed
+        vlost = c >= 1 && !wait_or_abort(&B->vfree, (c - 1) & 1, B, a.status);
         fence_async_smem();
         mbar_arrive(&B->ab_full[ps]);
         bar_named(kBarProd, kProdThreads);
-        // the raw v, beta buffer of chunk c - 1 is free once group B has moved them out
-        vlost = c >= 1 && !wait_or_abort(&B->vfree, (c - 1) & 1, B, a.status);
         if (c + 1 < nchunks && !vlost) {
             load_qk(a, smem, t0 + kChunk, rows_of(c + 1), h, ptid);
             load_vb(a, smem, t0 + kChunk, rows_of(c + 1), h, ptid, ps ^ 1);
