@@ -1145,7 +1145,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
 // the product. The map arrives transposed (row k of M^T is column k of M), so a warp reads
 // 512 contiguous bytes per k; each register is refilled with the next window's value as
 // soon as this window's has been read. The 8 partial products are summed through shared
-// memory.
+// memory. The products run as packed FP32 pairs of columns.
 constexpr int kCarryCols = 8;
 constexpr int kCarryWarps = kHeadDim / 16;
 constexpr int kCarryThreads = 32 * kCarryWarps;
@@ -1189,13 +1189,19 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
         for (int kk = 0; kk < 16; ++kk) {
             const float4 s0 = *reinterpret_cast<const float4 *>(&S[k0 + kk][0]);
             const float4 s1 = *reinterpret_cast<const float4 *>(&S[k0 + kk][4]);
-            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            const float2 sv[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
+                                  make_float2(s1.z, s1.w)};
             const float m[4] = {mv[kk].x, mv[kk].y, mv[kk].z, mv[kk].w};
             if (w + 2 < sp.wins_seq) mv[kk] = __ldcg(map_row(w + 1, kk));  // next window's row, a step ahead
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int c = 0; c < kCarryCols; ++c) acc[r][c] = fmaf(m[r], sv[c], acc[r][c]);
+                for (int c = 0; c < kCarryCols / 2; ++c) {
+                    const float2 x = __ffma2_rn(make_float2(m[r], m[r]), sv[c],
+                                                make_float2(acc[r][2 * c], acc[r][2 * c + 1]));
+                    acc[r][2 * c] = x.x;
+                    acc[r][2 * c + 1] = x.y;
+                }
         }
 #pragma unroll
         for (int c = 0; c < kCarryCols; ++c)
