@@ -84,8 +84,8 @@ constexpr int kStKt = kStW + 4 * 8192;            // tf32 [128 dk][32 tok]: Kr, 
 constexpr int kStBo = kStKt + 16384;              // tf32 [32 tok][32 tok]: Bo = Mqk T'
 constexpr int kStDec = kStBo + 4096;              // fp32 [128]: 2^G_last
 constexpr int kStageBytes = (kStDec + 512 + 1023) / 1024 * 1024;
-constexpr int kOst = kStage0 + 2 * kStageBytes;   // bf16 [32][136]: output staging
-constexpr int kPair = kOst + 32 * kRowB * 2;      // 3 x [48][136] bf16
+constexpr int kOst = kStage0 + 2 * kStageBytes;   // bf16x2 [16][128]: output staging (tokens t, 16 + t)
+constexpr int kPair = kOst + 16 * 128 * 4;        // 3 x [48][136] bf16
 constexpr int kPairQ = kPair;
 constexpr int kPairKL = kPairQ + 48 * kRowB * 2;
 constexpr int kPairKR = kPairKL + 48 * kRowB * 2;
@@ -889,23 +889,28 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         mbar_arrive(&B->oread[db]);
         // staged through shared memory for 16-byte row stores; the buffer is reused by the
         // next chunk only after the barrier that closes this iteration
-        uint8_t *const ost = smem + kOst;
+        // tokens t and 16 + t share a 32-bit word: ost[t][dv] = bf16x2(O[t][dv], O[16 + t][dv])
+        uint32_t *const ost = reinterpret_cast<uint32_t *>(smem + kOst);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            st_bf16(ost, t * kRowB + dv, o0[t]);
-            st_bf16(ost, (16 + t) * kRowB + dv, o1[t]);
-        }
+        for (int t = 0; t < 16; ++t) ost[t * kHeadDim + dv] = pack_bf16(o0[t], o1[t]);
         bar_named(kBarState, kStateThreads);
         const int t0 = bos + kChunk * c;
         const int L = min(kChunk, eos - t0);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 2; ++m) {
             const int idx = stid + kStateThreads * m;
-            const int row = idx >> 4, vec = idx & 15;
-            if (row < L) {
-                const uint4 v4 = *reinterpret_cast<const uint4 *>(ost + (row * kRowB + vec * 8) * 2);
-                *reinterpret_cast<uint4 *>(a.out + ((size_t)(t0 + row) * a.num_heads + h) * kHeadDim + vec * 8) = v4;
-            }
+            const int t = idx >> 4, vec = idx & 15;
+            const uint4 w0 = *reinterpret_cast<const uint4 *>(ost + t * kHeadDim + vec * 8);
+            const uint4 w1 = *reinterpret_cast<const uint4 *>(ost + t * kHeadDim + vec * 8 + 4);
+            __nv_bfloat16 *const orow = a.out + ((size_t)(t0 + t) * a.num_heads + h) * kHeadDim + vec * 8;
+            if (t < L)
+                *reinterpret_cast<uint4 *>(orow) =
+                    make_uint4(__byte_perm(w0.x, w0.y, 0x5410), __byte_perm(w0.z, w0.w, 0x5410),
+                               __byte_perm(w1.x, w1.y, 0x5410), __byte_perm(w1.z, w1.w, 0x5410));
+            if (16 + t < L)
+                *reinterpret_cast<uint4 *>(orow + (size_t)16 * a.num_heads * kHeadDim) =
+                    make_uint4(__byte_perm(w0.x, w0.y, 0x7632), __byte_perm(w0.z, w0.w, 0x7632),
+                               __byte_perm(w1.x, w1.y, 0x7632), __byte_perm(w1.z, w1.w, 0x7632));
         }
         alive = !bar_any(kBarState, kStateThreads, B->abort != 0);
     }
