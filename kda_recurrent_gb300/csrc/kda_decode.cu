@@ -78,6 +78,11 @@ struct StateVec<__nv_bfloat16> {
     }
 };
 
+// The two BF16 halves of a word as FP32 (low half first).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 struct TokenScalars {
     float qk;  // q_n . k_n
     float rq;  // q_n = rq q
@@ -344,28 +349,38 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
             if (t == 0 && gt < TT) s_beta[gt] = beta_mine;
             gbar();
             const TokenScalars ts = token_scalars(s_q, s_k, a);
-            float wk[8], wq[8];
+            // packed FP32 pairs of columns; the per-row vectors are read four rows at a time
+            float2 wk[4], wq[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) wk[e] = wq[e] = 0.0f;
-#pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-                const int row = 16 * rg + i;
-                float x[8];
-                StateVec<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(S + (row * kHeadDim + 8 * cb) * 2), x);
-                const float d = s_decay[row], kr = s_k[row], qr = s_q[row];
+            for (int e = 0; e < 4; ++e) wk[e] = wq[e] = make_float2(0.0f, 0.0f);
+#pragma unroll 2
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const int row0 = 16 * rg + 4 * i4;
+                const float4 d4 = *reinterpret_cast<const float4 *>(s_decay + row0);
+                const float4 k4 = *reinterpret_cast<const float4 *>(s_k + row0);
+                const float4 q4 = *reinterpret_cast<const float4 *>(s_q + row0);
+                const float dr[4] = {d4.x, d4.y, d4.z, d4.w}, kr[4] = {k4.x, k4.y, k4.z, k4.w};
+                const float qr[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float y = x[e] * d;
-                    wk[e] = fmaf(y, kr, wk[e]);
-                    wq[e] = fmaf(y, qr, wq[e]);
+                for (int r = 0; r < 4; ++r) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(S + ((row0 + r) * kHeadDim + 8 * cb) * 2);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 y = __fmul2_rn(bf16x2_to_float2(w[e]), make_float2(dr[r], dr[r]));
+                        wk[e] = __ffma2_rn(y, make_float2(kr[r], kr[r]), wk[e]);
+                        wq[e] = __ffma2_rn(y, make_float2(qr[r], qr[r]), wq[e]);
+                    }
                 }
             }
             float *const rk = s_red + rg * kHeadDim + 8 * cb;
             float *const rq = s_red + (8 + rg) * kHeadDim + 8 * cb;
-            *reinterpret_cast<float4 *>(rk) = make_float4(wk[0] * ts.rk, wk[1] * ts.rk, wk[2] * ts.rk, wk[3] * ts.rk);
-            *reinterpret_cast<float4 *>(rk + 4) = make_float4(wk[4] * ts.rk, wk[5] * ts.rk, wk[6] * ts.rk, wk[7] * ts.rk);
-            *reinterpret_cast<float4 *>(rq) = make_float4(wq[0] * ts.rq, wq[1] * ts.rq, wq[2] * ts.rq, wq[3] * ts.rq);
-            *reinterpret_cast<float4 *>(rq + 4) = make_float4(wq[4] * ts.rq, wq[5] * ts.rq, wq[6] * ts.rq, wq[7] * ts.rq);
+            const float2 rk2 = make_float2(ts.rk, ts.rk), rq2 = make_float2(ts.rq, ts.rq);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                reinterpret_cast<float2 *>(rk)[e] = __fmul2_rn(wk[e], rk2);
+                reinterpret_cast<float2 *>(rq)[e] = __fmul2_rn(wq[e], rq2);
+            }
             gbar();
             {  // column j = gt
                 float w_k = 0.0f, w_q = 0.0f;
@@ -379,23 +394,34 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
                 a.out[tok_index(item, t) * kHeadDim + gt] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
             }
             gbar();
-            float uv[8];
+            float2 uv[4];
             {
                 const float4 u0 = *reinterpret_cast<const float4 *>(s_u + 8 * cb);
                 const float4 u1 = *reinterpret_cast<const float4 *>(s_u + 8 * cb + 4);
-                uv[0] = u0.x, uv[1] = u0.y, uv[2] = u0.z, uv[3] = u0.w;
-                uv[4] = u1.x, uv[5] = u1.y, uv[6] = u1.z, uv[7] = u1.w;
+                uv[0] = make_float2(u0.x, u0.y), uv[1] = make_float2(u0.z, u0.w);
+                uv[2] = make_float2(u1.x, u1.y), uv[3] = make_float2(u1.z, u1.w);
             }
-#pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-                const int row = 16 * rg + i;
-                uint4 *const p = reinterpret_cast<uint4 *>(S + (row * kHeadDim + 8 * cb) * 2);
-                float x[8];
-                StateVec<__nv_bfloat16>::unpack(*p, x);
-                const float d = s_decay[row], kr = s_k[row] * ts.rk;
+#pragma unroll 2
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const int row0 = 16 * rg + 4 * i4;
+                const float4 d4 = *reinterpret_cast<const float4 *>(s_decay + row0);
+                const float4 k4 = *reinterpret_cast<const float4 *>(s_k + row0);
+                const float dr[4] = {d4.x, d4.y, d4.z, d4.w};
+                const float kr[4] = {k4.x * ts.rk, k4.y * ts.rk, k4.z * ts.rk, k4.w * ts.rk};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = fmaf(kr, uv[e], x[e] * d);
-                *p = StateVec<__nv_bfloat16>::pack(x);
+                for (int r = 0; r < 4; ++r) {
+                    uint4 *const p = reinterpret_cast<uint4 *>(S + ((row0 + r) * kHeadDim + 8 * cb) * 2);
+                    const uint4 raw = *p;
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = __ffma2_rn(make_float2(kr[r], kr[r]), uv[e],
+                                                    __fmul2_rn(bf16x2_to_float2(w[e]), make_float2(dr[r], dr[r])));
+                        o[e] = pack_bf16(x.x, x.y);
+                    }
+                    *p = make_uint4(o[0], o[1], o[2], o[3]);
+                }
             }
         }
         fence_async_smem();
