@@ -132,6 +132,12 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 128, "barrier block");
 
+// Programmatic dependent launch: let the next kernel of the stream start its launch now, and
+// wait until the previous kernel of the stream has completed and its writes are visible
+// (a no-op when the kernel was launched without the programmatic attribute).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -1123,6 +1129,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         if (kPass1) {
             state_loop_pass1(a, smem, B, tmem, nchunks, window_slot(a, chain, w, 1), window_slot(a, chain, w, 2));
         } else {
+            // the start state of a window is the carry's output; the operand and solve warps
+            // read only the inputs and start before the carry has finished
+            pdl_wait();
             const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
             const float *init = (w == 0) ? (a.init_state ? a.init_state + sbase : nullptr) : window_slot(a, chain, w, 0);
             float *fin = (w == sp.wins_seq - 1 && a.final_state) ? a.final_state + sbase : nullptr;
@@ -1162,6 +1171,7 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     const int chain = blockIdx.x / blocks;
     const int c0 = (blockIdx.x - chain * blocks) * kCarryCols;
     const int n = chain / a.num_heads;
+    pdl_launch_dependents();  // the output pass may start now; it waits for this grid on the device
     const WindowSpan sp = window_span(a, n, 0);
     if (sp.wins_seq <= 1) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1260,23 +1270,45 @@ WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_head
     return p;
 }
 
+// Launch on `stream` that may start while the previous kernel of the stream is finishing;
+// the kernel orders its dependent reads with griddepcontrol.wait.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       const PrefillArgs &a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     cudaError_t e = configure_once<false>();
     if (e != cudaSuccess) return e;
     const int64_t chains = (int64_t)a.num_seqs * a.num_heads;
     const int W = a.wins > 1 ? a.wins : 1;
-    if (W > 1) {
-        e = configure_once<true>();
-        if (e != cudaSuccess) return e;
-        kda_prefill_tc_kernel<true><<<(unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, 0, stream>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+    if (W == 1) {
+        kda_prefill_tc_kernel<false><<<(unsigned)chains, kThreadsTc, kSmemLaunch, stream>>>(a);
+        return cudaGetLastError();
     }
-    kda_prefill_tc_kernel<false><<<(unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream>>>(a);
-    return cudaGetLastError();
+    // window schedule: the window pass and the carry wait for everything before them on the
+    // stream; the output pass may start while the carry runs, its operand and solve warps
+    // working ahead while its state warps wait on the device for the carried start states
+    e = configure_once<true>();
+    if (e != cudaSuccess) return e;
+    kda_prefill_tc_kernel<true><<<(unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, 0, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kda_prefill_tc_kernel<false>, (unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream, a);
 }
 
 }  // namespace kda
