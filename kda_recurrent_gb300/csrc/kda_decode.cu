@@ -270,7 +270,10 @@ struct StreamShape {
     static __host__ __device__ uint32_t stage_bytes(int tokens) { return kItemBytes + kTokBytes * tokens; }
     static __host__ __device__ int stages(int tokens) {
         const int n = (int)((kStreamSmem - kFixed) / stage_bytes(tokens));
-        return n < kMaxStages ? n : kMaxStages;
+        // consecutive fills of a stage are NS items apart; with two compute groups taking
+        // alternate items, an even NS gives both fills to the same group, which waits for the
+        // earlier fill's phase before it can wait for the later one
+        return kGroups ? (n < kMaxStages ? n : kMaxStages) & ~1 : (n < kMaxStages ? n : kMaxStages);
     }
     static __host__ __device__ int smem(int tokens) { return stages(tokens) * stage_bytes(tokens) + kFixed; }
 };
