@@ -1159,14 +1159,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
 // the product. The map arrives transposed (row k of M^T is column k of M), so a warp reads
 // 512 contiguous bytes per k; each register is refilled with the next window's value as
 // soon as this window's has been read. The 8 partial products are summed through shared
-// memory. The products run as packed FP32 pairs of columns.
+// memory, and warp p also sums and rewrites rows [16p, 16p + 16) of S, the rows its next
+// window step reads, so one CTA barrier per window step suffices. The products run as
+// packed FP32 pairs of columns.
 constexpr int kCarryCols = 8;
 constexpr int kCarryWarps = kHeadDim / 16;
 constexpr int kCarryThreads = 32 * kCarryWarps;
 
+// Partial products, double-buffered by window step: [buffer][slice][column][row], rows padded
+// to 132 floats so that the two column halves a warp reads at once fall in different banks.
+constexpr int kCarryRowPad = kHeadDim + 4;
+constexpr int kCarryDynSmem = 2 * kCarryWarps * kCarryCols * kCarryRowPad * 4;
+
 __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const PrefillArgs a) {
     __shared__ __align__(16) float S[kHeadDim][kCarryCols];
-    __shared__ __align__(16) float part[kCarryWarps][kCarryCols][kHeadDim];  // [slice][column][row]
+    extern __shared__ __align__(16) float carry_dyn[];
+    auto part = reinterpret_cast<float (*)[kCarryWarps][kCarryCols][kCarryRowPad]>(carry_dyn);
     const int blocks = kHeadDim / kCarryCols;
     const int chain = blockIdx.x / blocks;
     const int c0 = (blockIdx.x - chain * blocks) * kCarryCols;
@@ -1176,25 +1184,28 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     if (sp.wins_seq <= 1) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
-    for (int idx = tid; idx < kHeadDim * kCarryCols; idx += kCarryThreads) {
-        const int i = idx / kCarryCols, cc = idx % kCarryCols;
-        S[i][cc] = a.init_state ? a.init_state[sbase + (size_t)i * kHeadDim + c0 + cc] : 0.0f;
-    }
     const int k0 = 16 * warp;
+    // warp w multiplies rows [k0, k0 + 16) of S and also reduces and rewrites exactly those
+    // rows, so between window steps it waits only for its own lanes
+    const int rr = k0 + (lane & 15), ch = lane >> 4;  // reduction: row rr, columns 4 ch .. 4 ch + 3
+    {
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (a.init_state) v = *reinterpret_cast<const float4 *>(a.init_state + sbase + (size_t)rr * kHeadDim + c0 + 4 * ch);
+        *reinterpret_cast<float4 *>(&S[rr][4 * ch]) = v;
+    }
     float4 mv[16];  // M^T[k0 + kk][4 lane .. 4 lane + 3]
     auto map_row = [&](int w, int kk) {
         return reinterpret_cast<const float4 *>(window_slot(a, chain, w, 2) + (size_t)(k0 + kk) * kHeadDim + 4 * lane);
     };
-    // reduction / output thread: row ri, columns 4 ch .. 4 ch + 3
-    const int ri = tid & (kHeadDim - 1), ch = tid >> 7;
     auto load_e = [&](int w) {
-        return __ldcg(reinterpret_cast<const float4 *>(window_slot(a, chain, w, 1) + (size_t)ri * kHeadDim + c0 + 4 * ch));
+        return __ldcg(reinterpret_cast<const float4 *>(window_slot(a, chain, w, 1) + (size_t)rr * kHeadDim + c0 + 4 * ch));
     };
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) mv[kk] = __ldcg(map_row(0, kk));
     float4 e4 = load_e(0);
-    __syncthreads();
+    __syncwarp();
     for (int w = 0; w + 1 < sp.wins_seq; ++w) {
+        const int b = w & 1;
         float acc[4][kCarryCols];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -1220,18 +1231,19 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
         }
 #pragma unroll
         for (int c = 0; c < kCarryCols; ++c)
-            *reinterpret_cast<float4 *>(&part[warp][c][4 * lane]) = make_float4(acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
-        __syncthreads();
+            *reinterpret_cast<float4 *>(&part[b][warp][c][4 * lane]) =
+                make_float4(acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
+        __syncthreads();  // every slice's partial products of step w are written
         float sum[4] = {e4.x, e4.y, e4.z, e4.w};
         if (w + 2 < sp.wins_seq) e4 = load_e(w + 1);
 #pragma unroll
         for (int p = 0; p < kCarryWarps; ++p)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) sum[c] += part[p][4 * ch + c][ri];
+            for (int c = 0; c < 4; ++c) sum[c] += part[b][p][4 * ch + c][rr];
         const float4 s4 = make_float4(sum[0], sum[1], sum[2], sum[3]);
-        *reinterpret_cast<float4 *>(&S[ri][4 * ch]) = s4;
-        *reinterpret_cast<float4 *>(window_slot(a, chain, w + 1, 0) + (size_t)ri * kHeadDim + c0 + 4 * ch) = s4;
-        __syncthreads();
+        *reinterpret_cast<float4 *>(&S[rr][4 * ch]) = s4;
+        *reinterpret_cast<float4 *>(window_slot(a, chain, w + 1, 0) + (size_t)rr * kHeadDim + c0 + 4 * ch) = s4;
+        __syncwarp();  // this warp's rows of S are rewritten
     }
 }
 
@@ -1243,6 +1255,9 @@ cudaError_t configure_once() {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
         e = cudaFuncSetAttribute(kda_prefill_tc_kernel<kPass1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch);
+        // the window pass is configured once per device, and with it the carry it feeds
+        if (e == cudaSuccess && kPass1)
+            e = cudaFuncSetAttribute(kda_window_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCarryDynSmem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
@@ -1305,7 +1320,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     kda_prefill_tc_kernel<true><<<(unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, 0, stream>>>(a);
+    kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, kCarryDynSmem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_pdl(kda_prefill_tc_kernel<false>, (unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream, a);
