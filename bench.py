@@ -234,7 +234,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
     ws = None if args.no_windows else K.prefill_workspace(len(pcfg.seqlens), pcfg.total_tokens, pcfg.num_heads,
                                                           device)
-    prefill_launches = 3 if ws is not None else 1  # window pass + carry + output pass, or the chunk loop
+    chains = len(pcfg.seqlens) * pcfg.num_heads
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    full_waves = chains // sms if ws is not None else 0  # chains ahead of a windowed tail, one CTA each
+    # window pass + carry + output pass (after the full waves' chunk loop, if any), or the chunk loop
+    prefill_launches = (3 + (full_waves > 0)) if ws is not None else 1
 
     def prefill_call():
         K.kda_prefill_ex(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta"], pin["cu_seqlens"],
@@ -309,6 +313,7 @@ def run_ours(args):
                     "traffic": (scaled_traffic(traffic, "kda_prefill_tc_kernel", prefill_units(pcfg))
                                 if ws is None else None),
                     "kernel": ("kda_prefill_tc_kernel" if ws is None else
+                               ("kda_prefill_tc_kernel full waves + " if full_waves else "") +
                                "kda_prefill_ex window schedule (window pass + carry + output pass)"), "peak_source": peak_src,
                     "algorithmic_bytes_per_launch": p_bytes,
                     "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -334,6 +339,8 @@ def run_ours(args):
                               "state_dtype": args.state_dtype},
                    "precision": "bf16 operands, tf32 state update, fp32 state and accumulation",
                    "prefill_schedule": ("sequential chunk loop" if ws is None else
+                                        (f"{full_waves} full waves of the chunk loop, then "
+                                         f"{chains - full_waves * sms} chains on " if full_waves else "") +
                                         f"windows ({ws.numel() >> 20} MiB workspace)"),
                    "l2": f"flushed between steps ({flush.numel() >> 20} MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},

@@ -114,8 +114,9 @@ int prefill_common(const void *q, const void *k, const void *v, const void *g_ra
     a.scale = scale;
     a.lower_bound = lower_bound;
     a.wins = 1;
-    a.win_chunks = 0;
     a.ws = nullptr;
+    a.seq_chains = 0;
+    a.chain_base = 0;
     a.ckpt = ckpt_every > 0 ? ckpt : nullptr;
     a.ckpt_offsets = ckpt_every > 0 ? ckpt_offsets : nullptr;
     a.ckpt_rows = ckpt_every > 0 ? ckpt_rows : 0;
@@ -128,8 +129,8 @@ int prefill_common(const void *q, const void *k, const void *v, const void *g_ra
         if (plan.wins > 1) {
             if (workspace_bytes < plan.ws_bytes) return KDA_ERR_INVALID_ARG;
             a.wins = plan.wins;
-            a.win_chunks = plan.win_chunks;
             a.ws = static_cast<float *>(workspace);
+            a.seq_chains = plan.seq_chains;
         }
     }
     cudaError_t e = device_status_ptr(&a.status);

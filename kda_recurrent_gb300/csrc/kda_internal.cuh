@@ -54,13 +54,17 @@ struct PrefillArgs {
     int32_t num_seqs, total_tokens, num_heads, gate_mode;
     float scale, lower_bound;
     DeviceStatus *status;
-    // Window schedule for short chain counts: each chain's chunks are cut into `wins`
-    // windows of `win_chunks` chunks (wins = 1: one window per chain). `ws` holds, per
+    // Window schedule for short chain counts: each chain's chunks are cut into up to `wins`
+    // windows of equal length (wins = 1: one window per chain). `ws` holds, per
     // (chain, window), three FP32 128 x 128 slots: the window's start state, and the
     // window's zero-start end state E and linear map M (S_end = M S_start + E), the map
-    // stored transposed (M^T, row-major).
-    int32_t wins, win_chunks;
+    // stored transposed (M^T, row-major). With `seq_chains` > 0 only the chains from
+    // seq_chains on are windowed (a tail shorter than one wave of the GPU); the chains
+    // before them run one CTA each. `chain_base` is the first chain of a launch, and the
+    // workspace is indexed from it.
+    int32_t wins;
     float *ws;
+    int32_t seq_chains, chain_base;
     // Optional intermediate states: every `ckpt_every` tokens (a multiple of the chunk),
     // the state after (j+1) * ckpt_every tokens of sequence n goes to row
     // ckpt_offsets[n] + j of ckpt [ckpt_rows][H][128][128] (ckpt_every = 0: none).
@@ -72,8 +76,9 @@ struct PrefillArgs {
 
 // Window plan of a prefill call on a device with `sms` multiprocessors.
 struct WindowPlan {
-    int32_t wins, win_chunks;
+    int32_t wins;
     int64_t ws_bytes;
+    int32_t seq_chains;  // chains before the windowed ones (0: all chains are windowed)
 };
 WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t sms);
 constexpr int64_t kWindowSlotBytes = 3LL * 128 * 128 * 4;

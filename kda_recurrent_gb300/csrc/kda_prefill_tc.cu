@@ -1045,23 +1045,31 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
 
 // ------------------------------------------------------------------ kernel
 
+// Shortest window of the window schedule, in chunks: each window adds a map to the carry.
+constexpr int kMinWindowChunks = 4;
+
 struct WindowSpan {
-    int bos, eos, w, wins_seq;
+    int bos, eos, w, wins_seq, lw;  // lw: chunks per window of this sequence
     bool live;
 };
 
-// Sequence bounds of chain `chain` (validated and clamped) and the span of window `w`.
-__device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, int w) {
+// Bounds of sequence n (validated and clamped; one caller per sequence, `report`, records
+// bad bounds) and the span of window `w` of it.
+__device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, int w, bool report) {
     int sb = a.cu_seqlens[n], se = a.cu_seqlens[n + 1];
     if (sb < 0 || se < sb || se > a.total_tokens) {
-        if (threadIdx.x == 0 && w == 0 && (blockIdx.x % (a.num_heads * max(a.wins, 1))) < (unsigned)max(a.wins, 1))
+        if (threadIdx.x == 0 && w == 0 && report)
             report_error(a.status, KDA_ERR_DEVICE_INPUT, n);
         sb = min(max(sb, 0), a.total_tokens);
         se = min(max(se, sb), a.total_tokens);
     }
+    // a sequence's chunks are split into at most a.wins windows of equal length, each at least
+    // kMinWindowChunks long (one window without the window schedule)
     const int chunks = (se - sb + kChunk - 1) / kChunk;
-    const int lw = a.win_chunks > 0 ? a.win_chunks : max(chunks, 1);
+    const int W = max(a.wins, 1);
+    const int lw = W > 1 ? max((chunks + W - 1) / W, kMinWindowChunks) : max(chunks, 1);
     WindowSpan sp;
+    sp.lw = lw;
     sp.wins_seq = max(1, (chunks + lw - 1) / lw);
     sp.w = w;
     sp.bos = sb + kChunk * lw * w;
@@ -1071,8 +1079,9 @@ __device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, i
     return sp;
 }
 
-__device__ __forceinline__ float *window_slot(const PrefillArgs &a, int chain, int w, int k) {
-    return a.ws + ((size_t)(chain * max(a.wins, 1) + w) * 3 + k) * (kHeadDim * kHeadDim);
+// Slot k of window w of the launch's chain `lc` (counted from a.chain_base).
+__device__ __forceinline__ float *window_slot(const PrefillArgs &a, int lc, int w, int k) {
+    return a.ws + ((size_t)(lc * max(a.wins, 1) + w) * 3 + k) * (kHeadDim * kHeadDim);
 }
 
 template <bool kPass1>
@@ -1084,13 +1093,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     const int warp = threadIdx.x >> 5;
     const int H = a.num_heads;
     const int W = max(a.wins, 1);
-    const int chain = blockIdx.x / W;
-    const int w = blockIdx.x - chain * W;
+    const int lc = blockIdx.x / W;  // chain of this launch
+    const int chain = a.chain_base + lc;
+    const int w = blockIdx.x - lc * W;
     const int n = chain / H;
     const int h = chain - n * H;
-    const WindowSpan sp = window_span(a, n, w);
+    const WindowSpan sp = window_span(a, n, w, h == 0);
+    // A window pass that follows a chunk loop over other chains may start while that loop's
+    // last chains still run; it ends only after them, so every later launch is ordered after
+    // both (griddepcontrol.wait returns at once when nothing precedes the grid).
+    if (!kPass1) pdl_launch_dependents();
     // The window pass covers every window but the last (its map is never needed).
-    if (kPass1 ? (w >= sp.wins_seq - 1) : !sp.live) return;
+    if (kPass1 ? (w >= sp.wins_seq - 1) : !sp.live) {
+        if (kPass1) pdl_wait();
+        return;
+    }
     const int bos = sp.bos, eos = sp.eos;
     const int nchunks = (eos - bos + kChunk - 1) / kChunk;
 
@@ -1127,15 +1144,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         solve_loop<kPass1>(a, smem, B, tmem, nchunks);
     } else {
         if (kPass1) {
-            state_loop_pass1(a, smem, B, tmem, nchunks, window_slot(a, chain, w, 1), window_slot(a, chain, w, 2));
+            state_loop_pass1(a, smem, B, tmem, nchunks, window_slot(a, lc, w, 1), window_slot(a, lc, w, 2));
         } else {
             // the start state of a window is the carry's output; the operand and solve warps
             // read only the inputs and start before the carry has finished
             pdl_wait();
             const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
-            const float *init = (w == 0) ? (a.init_state ? a.init_state + sbase : nullptr) : window_slot(a, chain, w, 0);
+            const float *init = (w == 0) ? (a.init_state ? a.init_state + sbase : nullptr) : window_slot(a, lc, w, 0);
             float *fin = (w == sp.wins_seq - 1 && a.final_state) ? a.final_state + sbase : nullptr;
-            const int chunk_base = (a.win_chunks > 0) ? a.win_chunks * w : 0;
+            const int chunk_base = sp.lw * w;
             state_loop(a, smem, B, tmem, n, h, bos, eos, nchunks, chunk_base, init, fin);
         }
         if (B->abort != 0 && warp == kFirstStateWarp && (threadIdx.x & 31) == 0) {
@@ -1149,6 +1166,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     __syncthreads();
     tc_fence_after();
     if (warp == kFirstStateWarp) tmem_dealloc(tmem, kTmemCols);
+    if (kPass1) pdl_wait();
 }
 
 // ------------------------------------------------------------------ window carry
@@ -1176,11 +1194,12 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     extern __shared__ __align__(16) float carry_dyn[];
     auto part = reinterpret_cast<float (*)[kCarryWarps][kCarryCols][kCarryRowPad]>(carry_dyn);
     const int blocks = kHeadDim / kCarryCols;
-    const int chain = blockIdx.x / blocks;
-    const int c0 = (blockIdx.x - chain * blocks) * kCarryCols;
+    const int lc = blockIdx.x / blocks;  // chain of this launch
+    const int chain = a.chain_base + lc;
+    const int c0 = (blockIdx.x - lc * blocks) * kCarryCols;
     const int n = chain / a.num_heads;
     pdl_launch_dependents();  // the output pass may start now; it waits for this grid on the device
-    const WindowSpan sp = window_span(a, n, 0);
+    const WindowSpan sp = window_span(a, n, 0, false);
     if (sp.wins_seq <= 1) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
@@ -1195,10 +1214,10 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     }
     float4 mv[16];  // M^T[k0 + kk][4 lane .. 4 lane + 3]
     auto map_row = [&](int w, int kk) {
-        return reinterpret_cast<const float4 *>(window_slot(a, chain, w, 2) + (size_t)(k0 + kk) * kHeadDim + 4 * lane);
+        return reinterpret_cast<const float4 *>(window_slot(a, lc, w, 2) + (size_t)(k0 + kk) * kHeadDim + 4 * lane);
     };
     auto load_e = [&](int w) {
-        return __ldcg(reinterpret_cast<const float4 *>(window_slot(a, chain, w, 1) + (size_t)rr * kHeadDim + c0 + 4 * ch));
+        return __ldcg(reinterpret_cast<const float4 *>(window_slot(a, lc, w, 1) + (size_t)rr * kHeadDim + c0 + 4 * ch));
     };
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) mv[kk] = __ldcg(map_row(0, kk));
@@ -1242,7 +1261,7 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
             for (int c = 0; c < 4; ++c) sum[c] += part[b][p][4 * ch + c][rr];
         const float4 s4 = make_float4(sum[0], sum[1], sum[2], sum[3]);
         *reinterpret_cast<float4 *>(&S[rr][4 * ch]) = s4;
-        *reinterpret_cast<float4 *>(window_slot(a, chain, w + 1, 0) + (size_t)rr * kHeadDim + c0 + 4 * ch) = s4;
+        *reinterpret_cast<float4 *>(window_slot(a, lc, w + 1, 0) + (size_t)rr * kHeadDim + c0 + 4 * ch) = s4;
         __syncwarp();  // this warp's rows of S are rewritten
     }
 }
@@ -1273,15 +1292,18 @@ WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_head
     WindowPlan p = {1, 0, 0};
     const int64_t chains = (int64_t)num_seqs * num_heads;
     const int64_t max_chunks = ((int64_t)total_tokens + kChunk - 1) / kChunk;  // bound on any one sequence
-    constexpr int64_t kMinWindowChunks = 4;
-    if (chains <= 0 || sms <= 0 || chains * 3 > sms) return p;
-    int64_t wins = std::min<int64_t>(sms / chains, max_chunks / kMinWindowChunks);
+    if (chains <= 0 || sms <= 0) return p;
+    // Chains run one CTA each, a wave of `sms` at a time. When the last wave would hold at
+    // most a third of the GPU (or all chains fit in such a wave), those chains are cut into
+    // windows instead, at least three per chain, to fill the GPU; the full waves before them
+    // are unchanged. Each sequence's window length follows from its own length on the device.
+    const int64_t tail = chains % sms;
+    if (tail == 0 || tail * 3 > sms) return p;
+    const int64_t wins = std::min<int64_t>(sms / tail, max_chunks / kMinWindowChunks);
     if (wins < 3) return p;
-    const int64_t lw = (max_chunks + wins - 1) / wins;
-    wins = (max_chunks + lw - 1) / lw;
     p.wins = (int32_t)wins;
-    p.win_chunks = (int32_t)lw;
-    p.ws_bytes = chains * wins * kWindowSlotBytes;
+    p.ws_bytes = tail * wins * kWindowSlotBytes;
+    p.seq_chains = (int32_t)(chains - tail);
     return p;
 }
 
@@ -1303,27 +1325,43 @@ cudaError_t launch_pdl(void (*kernel)(Args...), unsigned grid, unsigned block, s
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
+cudaError_t launch_prefill_tc(const PrefillArgs &args, cudaStream_t stream) {
     cudaError_t e = configure_once<false>();
     if (e != cudaSuccess) return e;
-    const int64_t chains = (int64_t)a.num_seqs * a.num_heads;
-    const int W = a.wins > 1 ? a.wins : 1;
-    if (W == 1) {
-        kda_prefill_tc_kernel<false><<<(unsigned)chains, kThreadsTc, kSmemLaunch, stream>>>(a);
-        return cudaGetLastError();
+    const int64_t all_chains = (int64_t)args.num_seqs * args.num_heads;
+    const int W = args.wins > 1 ? args.wins : 1;
+    // chains [0, seq) one CTA each, then chains [seq, all) on the window schedule
+    const int64_t seq = W == 1 ? all_chains : args.seq_chains;
+    if (seq > 0) {
+        PrefillArgs s = args;
+        s.wins = 1;
+        s.chain_base = 0;
+        kda_prefill_tc_kernel<false><<<(unsigned)seq, kThreadsTc, kSmemLaunch, stream>>>(s);
+        e = cudaGetLastError();
+        if (e != cudaSuccess || W == 1) return e;
     }
-    // window schedule: the window pass and the carry wait for everything before them on the
-    // stream; the output pass may start while the carry runs, its operand and solve warps
-    // working ahead while its state warps wait on the device for the carried start states
+    PrefillArgs a = args;
+    a.chain_base = (int32_t)seq;
+    const int64_t chains = all_chains - seq;
+    // Window schedule. Alone, the window pass waits for everything before it on the stream;
+    // after a chunk loop over other chains it may start in the SMs that loop's last chains
+    // leave free, and it ends after that loop. The carry follows the window pass; the output
+    // pass may start while the carry runs, its operand and solve warps working ahead while
+    // its state warps wait on the device for the carried start states.
     e = configure_once<true>();
     if (e != cudaSuccess) return e;
-    kda_prefill_tc_kernel<true><<<(unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream>>>(a);
-    e = cudaGetLastError();
+    const unsigned ctas = (unsigned)(chains * W);
+    if (seq > 0) {
+        e = launch_pdl(kda_prefill_tc_kernel<true>, ctas, kThreadsTc, kSmemLaunch, stream, a);
+    } else {
+        kda_prefill_tc_kernel<true><<<ctas, kThreadsTc, kSmemLaunch, stream>>>(a);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, kCarryDynSmem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_pdl(kda_prefill_tc_kernel<false>, (unsigned)(chains * W), kThreadsTc, kSmemLaunch, stream, a);
+    return launch_pdl(kda_prefill_tc_kernel<false>, ctas, kThreadsTc, kSmemLaunch, stream, a);
 }
 
 }  // namespace kda

@@ -10,7 +10,7 @@ import torch
 
 import kda_recurrent_gb300 as K
 import kda_synth as S
-from helpers import assert_out_close, assert_state_close, oracle_prefill, rel_l2
+from helpers import assert_out_close, assert_state_close, oracle_prefill, rel_l2, slice_problem
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -110,3 +110,32 @@ def test_workspace_rules():
     K.kda_prefill_ex(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"], None, out_b, fin_b,
                      SCALE, -5.0, workspace=None)
     assert torch.equal(out_a, out_b) and torch.equal(fin_a, fin_b)
+
+
+def test_windowed_tail_after_full_waves():
+    """More chains than SMs with a short last wave: the full waves run one CTA per chain and
+    only the last chains are windowed. The split falls inside the second sequence, so one
+    sequence's heads run on both schedules."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tail = 4
+    H = (sms + tail) // 2
+    tail = 2 * H - sms
+    lens = [900, 1500]
+    inp = S.prefill_inputs(lens, H, seed=35, init_std=0.02)
+    assert K.kda_prefill_workspace_size(2, sum(lens), H) > 0
+    out, fin = windowed(inp, lower_bound=-5.0, gate_mode="lower_bound")
+    d = to_dev(inp)
+    out_s, fin_s = K.prefill(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], d["cu_seqlens"], d["init_state"],
+                             scale=SCALE, lower_bound=-5.0)
+    # the chains of the full waves take the sequential kernel unchanged: bitwise equal
+    first = sms - H  # heads of sequence 1 that precede the windowed tail
+    assert torch.equal(out[:lens[0]], out_s[:lens[0]].cpu()) and torch.equal(fin[0], fin_s[0].cpu())
+    assert torch.equal(out[lens[0]:, :first], out_s[lens[0]:, :first].cpu())
+    assert torch.equal(fin[1, :first], fin_s[1, :first].cpu())
+    # the windowed tail against the oracle, and a few heads of the full waves
+    heads = [0, first - 1] + list(range(first, H))
+    sub = slice_problem(inp, heads=heads)
+    ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=-5.0, gate_mode="lower_bound")
+    assert_out_close(out[:, heads], ref_out)
+    assert_state_close(fin[:, heads], ref_fin)
+    assert tail == H - first
