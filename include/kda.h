@@ -114,7 +114,8 @@ KDA_API int kda_prefill(const void *q, const void *k, const void *v, const void 
 
 /*
  * kda_prefill_workspace_size -- bytes of device workspace kda_prefill_ex uses for a call
- * of this shape; 0 means it would not use any (the chains already fill the GPU).
+ * of this shape; 0 means it would not use any (the chains fill whole waves of the GPU, or
+ * leave a last wave of more than a third of it).
  *   sm_count  multiprocessors of the device the call will run on; 0 = ask the current
  *             device (a CUDA call). With sm_count > 0 this is pure host arithmetic.
  * Returns the byte count, or a negative kda_status (KDA_ERR_INVALID_ARG for bad sizes,
@@ -126,7 +127,9 @@ KDA_API int64_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_token
 /*
  * kda_prefill_ex -- kda_prefill with a caller-owned device workspace (16-byte aligned).
  * When the (sequence, head) chains are too few to fill the GPU, each chain's chunks are
- * cut into windows that run in parallel, in the spirit of the windowed "affine
+ * cut into windows that run in parallel; with more chains than multiprocessors, the
+ * same is done for the chains of a last wave that holds at most a third of the GPU,
+ * after the full waves have run one CTA per chain. This follows the windowed "affine
  * composite" of FlashInfer PR #5573 ("1. Composite schedule"): a window pass computes,
  * from a zero start, each window's end state E and linear map M (S_end = M S_start + E);
  * an FP32 carry pass walks the windows of each chain; the output pass then reruns every

@@ -21,7 +21,7 @@
 namespace kda {
 namespace {
 
-// Scratch of the window schedule: 32 MiB. The window plan keeps (chains x windows) at or
+// Scratch of the window schedule: 32 MiB. The window plan keeps (windowed chains x windows) at or
 // below the SM count, and each (chain, window) needs 192 KiB, so this covers every plan
 // on GPUs with up to 170 SMs (GB300 has 152).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
