@@ -1079,6 +1079,40 @@ __device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, i
     return sp;
 }
 
+// Launch order of the chains. CTAs start roughly in index order, one per SM, so a batch of
+// unequal sequences finishes soonest when the longest start first (the longest-processing-
+// time-first rule of list scheduling). Position p of the order is head p % H of the
+// sequence ranked p / H by length, longest first, ties by index; the ranks are a permutation
+// for any cu_seqlens, so every chain runs exactly once. Batches of more than kRankedSeqs
+// sequences keep index order (ranking them would cost each CTA more than it saves).
+constexpr int kRankedSeqs = 256;
+
+// Sequence of rank j; every thread of the CTA calls it (it holds three CTA barriers) with
+// `scratch` pointing to kRankedSeqs + 1 ints of shared memory that nothing else uses until
+// it returns.
+__device__ __forceinline__ int seq_of_rank(const PrefillArgs &a, int j, int *scratch) {
+    const int N = a.num_seqs;
+    if (N <= 1 || N > kRankedSeqs) return j;
+    int *len = scratch;
+    int *pick = scratch + kRankedSeqs;
+    for (int i = threadIdx.x; i < N; i += blockDim.x)  // wrapping difference: any input orders
+        len[i] = (int)((unsigned)__ldg(a.cu_seqlens + i + 1) - (unsigned)__ldg(a.cu_seqlens + i));
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        const int li = len[i];
+        int r = 0;
+        for (int m = 0; m < N; ++m) {
+            const int lm = len[m];
+            r += (lm > li) | ((lm == li) & (m < i));
+        }
+        if (r == j) *pick = i;
+    }
+    __syncthreads();
+    const int n = *pick;
+    __syncthreads();
+    return n;
+}
+
 // Slot k of window w of the launch's chain `lc` (counted from a.chain_base).
 __device__ __forceinline__ float *window_slot(const PrefillArgs &a, int lc, int w, int k) {
     return a.ws + ((size_t)(lc * max(a.wins, 1) + w) * 3 + k) * (kHeadDim * kHeadDim);
@@ -1094,10 +1128,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     const int H = a.num_heads;
     const int W = max(a.wins, 1);
     const int lc = blockIdx.x / W;  // chain of this launch
-    const int chain = a.chain_base + lc;
+    const int pos = a.chain_base + lc;  // position in the launch order
     const int w = blockIdx.x - lc * W;
-    const int n = chain / H;
-    const int h = chain - n * H;
+    const int h = pos % H;
+    // the stage area is free until the pipeline starts
+    const int n = seq_of_rank(a, pos / H, reinterpret_cast<int *>(smem + kStage0));
+    const int chain = n * H + h;
     const WindowSpan sp = window_span(a, n, w, h == 0);
     // A window pass that follows a chunk loop over other chains may start while that loop's
     // last chains still run; it ends only after them, so every later launch is ordered after
@@ -1195,10 +1231,11 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     auto part = reinterpret_cast<float (*)[kCarryWarps][kCarryCols][kCarryRowPad]>(carry_dyn);
     const int blocks = kHeadDim / kCarryCols;
     const int lc = blockIdx.x / blocks;  // chain of this launch
-    const int chain = a.chain_base + lc;
+    const int pos = a.chain_base + lc;  // position in the launch order
     const int c0 = (blockIdx.x - lc * blocks) * kCarryCols;
-    const int n = chain / a.num_heads;
     pdl_launch_dependents();  // the output pass may start now; it waits for this grid on the device
+    const int n = seq_of_rank(a, pos / a.num_heads, reinterpret_cast<int *>(carry_dyn));
+    const int chain = n * a.num_heads + pos % a.num_heads;
     const WindowSpan sp = window_span(a, n, 0, false);
     if (sp.wins_seq <= 1) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

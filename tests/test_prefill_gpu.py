@@ -125,6 +125,32 @@ def test_varlen_equals_separate_calls_bitwise():
         assert torch.equal(f[0], fin[n])
 
 
+@pytest.mark.parametrize("lens", [
+    [64, 64, 0, 130, 64, 7, 130, 0, 33, 7],           # ties: chains start longest first, ties by index
+    [3 * (i % 7) + 32 * (i % 3) for i in range(300)],  # more sequences than are ranked: index order
+])
+def test_launch_order_runs_every_chain_once(lens):
+    """Each chain's result is independent of when its CTA starts: bitwise equal to a call on
+    that sequence alone, so every (sequence, head) ran exactly once on its own data."""
+    inp = to_dev(S.prefill_inputs(lens, 2, seed=28, init_std=0.02))
+    args = dict(scale=SCALE, lower_bound=-5.0, gate_mode="lower_bound")
+    out, fin = K.prefill(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"],
+                         inp["init_state"], **args)
+    assert K.kda_device_status()[0] == K.KDA_OK
+    cu = inp["cu_seqlens"].tolist()
+    for n in sorted(set(range(0, len(lens), max(1, len(lens) // 12))) | {len(lens) - 1}):
+        sl = slice(cu[n], cu[n + 1])
+        c1 = torch.tensor([0, lens[n]], dtype=torch.int32, device=DEV)
+        o, f = K.prefill(inp["q"][sl].contiguous(), inp["k"][sl].contiguous(), inp["v"][sl].contiguous(),
+                         inp["g_raw"][sl].contiguous(), inp["beta"][sl].contiguous(), c1,
+                         inp["init_state"][n:n + 1].contiguous(), **args)
+        assert torch.equal(o, out[sl]) and torch.equal(f[0], fin[n]), n
+    sub = slice_problem({k: v.cpu() if isinstance(v, torch.Tensor) else v for k, v in inp.items()})
+    ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, **{k: v for k, v in args.items() if k != "scale"})
+    assert_out_close(out.cpu(), ref_out)
+    assert_state_close(fin.cpu(), ref_fin)
+
+
 def test_zero_length_sequence_copies_initial_state():
     inp = to_dev(S.prefill_inputs([0, 33, 0], 2, seed=23, init_std=0.02))
     out, fin = K.prefill(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"],

@@ -114,13 +114,13 @@ def test_workspace_rules():
 
 def test_windowed_tail_after_full_waves():
     """More chains than SMs with a short last wave: the full waves run one CTA per chain and
-    only the last chains are windowed. The split falls inside the second sequence, so one
-    sequence's heads run on both schedules."""
+    only the last chains are windowed. Chains start longest sequence first, so the split falls
+    inside the shorter (second) sequence, whose heads then run on both schedules."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tail = 4
     H = (sms + tail) // 2
     tail = 2 * H - sms
-    lens = [900, 1500]
+    lens = [1500, 900]
     inp = S.prefill_inputs(lens, H, seed=35, init_std=0.02)
     assert K.kda_prefill_workspace_size(2, sum(lens), H) > 0
     out, fin = windowed(inp, lower_bound=-5.0, gate_mode="lower_bound")
