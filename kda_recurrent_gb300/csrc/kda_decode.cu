@@ -241,7 +241,7 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_but_newest() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
@@ -434,8 +434,10 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
 
 // One CTA per SM: warps 0-7 update states; warp 8 (lane 0) moves them. Stage s is filled by
 // bulk copies that complete `full[s]`; the compute warps arrive on `done[s]` once the
-// updated state is back in the stage; the producer then stores it with a bulk copy and,
-// once that copy has read the stage, refills it with the state NS items ahead. With
+// updated state is back in the stage; the producer then stores it with a bulk copy. It
+// refills a stage with the state NS items ahead one item later, once the store has read
+// the stage: waiting for that read right after issuing the store kept the producer from
+// issuing anything else for the length of the read. With
 // several tokens per row the state stays in registers while its tokens are applied in
 // order, and is stored once.
 template <typename T>
@@ -529,11 +531,13 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
 #pragma unroll
                 for (uint32_t p = 0; p < SS::kItemBytes; p += SS::kPiece)
                     bulk_store(dst + p, smem_addr(stages + (size_t)st * stage_bytes + p), SS::kPiece);
-                bulk_commit();
             }
-            if (j + NS < mine) {
-                bulk_wait_read_all();  // the stage's store has read it
-                issue(j + NS);
+            bulk_commit();  // one group per item, empty for a skipped one
+            // the stage of the previous item is refilled once its store has read it, which
+            // has had this item's wait to happen in
+            if (j >= 1 && j - 1 + NS < mine) {
+                bulk_wait_read_but_newest();
+                issue(j - 1 + NS);
             }
         }
         bulk_wait_all();
