@@ -319,7 +319,7 @@ def run_ours(args):
                     "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": round(p_tflops / peaks["bf16_tflops"], 5),
                                "flop_per_launch": prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD}}
-    d_kernel = decode_kernel_name(args.decode_rows * dcfg.num_heads, sms)
+    d_kernel = decode_kernel_name(args.decode_rows * dcfg.num_heads, sms, args.state_dtype)
     decode_roof = {"bound": "hbm", "achieved": round(d_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                    "frac": round(d_gbs / peaks["hbm_gbs"], 5),
                    "traffic": scaled_traffic(traffic, f"{d_kernel}<{args.state_dtype}>",
@@ -456,10 +456,11 @@ def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws):
             "on three streams; two device copies of inputs and outputs"}
 
 
-def decode_kernel_name(items: int, sms: int) -> str:
+def decode_kernel_name(items: int, sms: int, state_dtype: str = "f32") -> str:
     """The decode kernel the library launches for one token per row: the streaming
-    schedule from 4 (row, head) items per SM on, the register schedule below that."""
-    return "kda_decode_stream_kernel" if items >= 4 * sms else "kda_decode_kernel"
+    schedule from 4 (FP32 states) or 3 (BF16) (row, head) items per SM on, the register
+    schedule below that."""
+    return "kda_decode_stream_kernel" if items >= (4 if state_dtype == "f32" else 3) * sms else "kda_decode_kernel"
 
 
 def source_digest(kernel_file: str) -> str:

@@ -679,8 +679,11 @@ int pick_decode_width(int64_t items) {
     return 32;
 }
 
-// Items from which the streaming schedule takes over (several per SM, so its ring fills).
-constexpr int kStreamItemsPerSm = 4;
+// Items per SM from which the streaming schedule takes over (several per SM, so that its
+// ring fills): measured crossovers of the two schedules, BF16 states between 1.7 and 3.4
+// items per SM, FP32 states near 3.4.
+constexpr int kStreamItemsPerSmF32 = 4;
+constexpr int kStreamItemsPerSmBF16 = 3;
 
 }  // namespace
 
@@ -690,7 +693,8 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (a.tokens > 1 || items >= (int64_t)kStreamItemsPerSm * sms) {
+    const int per_sm = a.state_dtype == KDA_STATE_F32 ? kStreamItemsPerSmF32 : kStreamItemsPerSmBF16;
+    if (a.tokens > 1 || items >= (int64_t)per_sm * sms) {
         if (a.state_dtype == KDA_STATE_F32) return launch_decode_stream<float>(a, stream, sms);
         return launch_decode_stream<__nv_bfloat16>(a, stream, sms);
     }

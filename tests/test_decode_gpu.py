@@ -53,7 +53,7 @@ def test_decode_sweep_pool16384(state_dtype):
 
 
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("rows", [3, 37, 300])
+@pytest.mark.parametrize("rows", [3, 37, 160, 300])  # 480 items: BF16 states stream, FP32 ones do not
 def test_decode_softplus_small_pool(state_dtype, rows):
     pool = S.state_pool(512, 3, state_dtype, std=0.05, seed=9, device=DEV)
     run_and_check(pool, rows, 3, 9, lower_bound=0.0, gate_mode="softplus")
