@@ -237,8 +237,8 @@ def run_ours(args):
     chains = len(pcfg.seqlens) * pcfg.num_heads
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     full_waves = chains // sms if ws is not None else 0  # chains ahead of a windowed tail, one CTA each
-    # window pass + carry + output pass (after the full waves' chunk loop, if any), or the chunk loop
-    prefill_launches = (3 + (full_waves > 0)) if ws is not None else 1
+    # chunk loop (full waves and window 0) + window pass + carry + output pass, or the chunk loop
+    prefill_launches = 4 if ws is not None else 1
 
     def prefill_call():
         K.kda_prefill_ex(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta"], pin["cu_seqlens"],
@@ -314,7 +314,7 @@ def run_ours(args):
                                 if ws is None else None),
                     "kernel": ("kda_prefill_tc_kernel" if ws is None else
                                ("kda_prefill_tc_kernel full waves + " if full_waves else "") +
-                               "kda_prefill_ex window schedule (window pass + carry + output pass)"), "peak_source": peak_src,
+                               "kda_prefill_ex window schedule (window 0, window pass, carry, output pass)"), "peak_source": peak_src,
                     "algorithmic_bytes_per_launch": p_bytes,
                     "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": round(p_tflops / peaks["bf16_tflops"], 5),

@@ -116,7 +116,9 @@ int prefill_common(const void *q, const void *k, const void *v, const void *g_ra
     a.wins = 1;
     a.ws = nullptr;
     a.seq_chains = 0;
-    a.chain_base = 0;
+    a.seq_ctas = 0;
+    a.win_first = 0;
+    a.win_count = 1;
     a.ckpt = ckpt_every > 0 ? ckpt : nullptr;
     a.ckpt_offsets = ckpt_every > 0 ? ckpt_offsets : nullptr;
     a.ckpt_rows = ckpt_every > 0 ? ckpt_rows : 0;

@@ -54,17 +54,20 @@ struct PrefillArgs {
     int32_t num_seqs, total_tokens, num_heads, gate_mode;
     float scale, lower_bound;
     DeviceStatus *status;
-    // Window schedule for short chain counts: each chain's chunks are cut into up to `wins`
-    // windows of equal length (wins = 1: one window per chain). `ws` holds, per
-    // (chain, window), three FP32 128 x 128 slots: the window's start state, and the
-    // window's zero-start end state E and linear map M (S_end = M S_start + E), the map
-    // stored transposed (M^T, row-major). With `seq_chains` > 0 only the chains from
-    // seq_chains on are windowed (a tail shorter than one wave of the GPU); the chains
-    // before them run one CTA each. `chain_base` is the first chain of a launch, and the
-    // workspace is indexed from it.
+    // Window schedule: the chains from launch position `seq_chains` on have their chunks cut
+    // into up to `wins` windows of equal length (wins = 1: no windows). Window 0 runs from
+    // the initial state like a whole chain and leaves its end state as window 1's start; a
+    // window pass computes the end state E (from a zero start) and the linear map M
+    // (S_end = M S_start + E) of windows 1 .. wins - 2; the carry chains the start states of
+    // windows 2 .. wins - 1; an output pass reruns windows 1 .. wins - 1 from them. `ws`
+    // holds these FP32 128 x 128 slots per windowed chain (window_slot).
     int32_t wins;
     float *ws;
-    int32_t seq_chains, chain_base;
+    int32_t seq_chains;
+    // Per launch: CTAs [0, seq_ctas) run whole chains (positions 0 .. seq_ctas - 1); each later
+    // group of win_count CTAs runs windows win_first .. win_first + win_count - 1 of the next
+    // windowed chain.
+    int32_t seq_ctas, win_first, win_count;
     // Optional intermediate states: every `ckpt_every` tokens (a multiple of the chunk),
     // the state after (j+1) * ckpt_every tokens of sequence n goes to row
     // ckpt_offsets[n] + j of ckpt [ckpt_rows][H][128][128] (ckpt_every = 0: none).
@@ -81,7 +84,10 @@ struct WindowPlan {
     int32_t seq_chains;  // chains before the windowed ones (0: all chains are windowed)
 };
 WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t sms);
-constexpr int64_t kWindowSlotBytes = 3LL * 128 * 128 * 4;
+constexpr int64_t kStateBytes = 128LL * 128 * 4;
+// Slots of one windowed chain with `wins` windows: start states of windows 1 .. wins - 1, and
+// E and M of windows 1 .. wins - 2.
+__host__ __device__ constexpr int64_t window_slots(int64_t wins) { return 3 * wins - 5; }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);  // windows when a.wins > 1

@@ -1055,7 +1055,7 @@ struct WindowSpan {
 
 // Bounds of sequence n (validated and clamped; one caller per sequence, `report`, records
 // bad bounds) and the span of window `w` of it.
-__device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, int w, bool report) {
+__device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, int w, int W, bool report) {
     int sb = a.cu_seqlens[n], se = a.cu_seqlens[n + 1];
     if (sb < 0 || se < sb || se > a.total_tokens) {
         if (threadIdx.x == 0 && w == 0 && report)
@@ -1063,10 +1063,9 @@ __device__ __forceinline__ WindowSpan window_span(const PrefillArgs &a, int n, i
         sb = min(max(sb, 0), a.total_tokens);
         se = min(max(se, sb), a.total_tokens);
     }
-    // a sequence's chunks are split into at most a.wins windows of equal length, each at least
-    // kMinWindowChunks long (one window without the window schedule)
+    // a sequence's chunks are split into at most W windows of equal length, each at least
+    // kMinWindowChunks long (W = 1: one window)
     const int chunks = (se - sb + kChunk - 1) / kChunk;
-    const int W = max(a.wins, 1);
     const int lw = W > 1 ? max((chunks + W - 1) / W, kMinWindowChunks) : max(chunks, 1);
     WindowSpan sp;
     sp.lw = lw;
@@ -1113,9 +1112,13 @@ __device__ __forceinline__ int seq_of_rank(const PrefillArgs &a, int j, int *scr
     return n;
 }
 
-// Slot k of window w of the launch's chain `lc` (counted from a.chain_base).
+// Slot of windowed chain `lc` (counted from position a.seq_chains): k = 0, the start state of
+// window w (w = 1 .. wins - 1); k = 1 and 2, the end state E and the map M of window w
+// (w = 1 .. wins - 2).
 __device__ __forceinline__ float *window_slot(const PrefillArgs &a, int lc, int w, int k) {
-    return a.ws + ((size_t)(lc * max(a.wins, 1) + w) * 3 + k) * (kHeadDim * kHeadDim);
+    const int W = a.wins;
+    const int idx = (k == 0) ? w - 1 : (k == 1 ? (W - 1) + (w - 1) : (W - 1) + (W - 2) + (w - 1));
+    return a.ws + ((size_t)lc * (size_t)window_slots(W) + (size_t)idx) * (kHeadDim * kHeadDim);
 }
 
 template <bool kPass1>
@@ -1126,15 +1129,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     Bars *B = reinterpret_cast<Bars *>(smem + kBars);
     const int warp = threadIdx.x >> 5;
     const int H = a.num_heads;
-    const int W = max(a.wins, 1);
-    const int lc = blockIdx.x / W;  // chain of this launch
-    const int pos = a.chain_base + lc;  // position in the launch order
-    const int w = blockIdx.x - lc * W;
+    // a whole chain, or window w of windowed chain lc
+    const bool windowed = (int)blockIdx.x >= a.seq_ctas;
+    int pos = blockIdx.x, w = 0, lc = 0;  // pos: position in the launch order
+    if (windowed) {
+        const int b = (int)blockIdx.x - a.seq_ctas;
+        lc = b / a.win_count;
+        w = a.win_first + (b - lc * a.win_count);
+        pos = a.seq_chains + lc;
+    }
     const int h = pos % H;
     // the stage area is free until the pipeline starts
     const int n = seq_of_rank(a, pos / H, reinterpret_cast<int *>(smem + kStage0));
     const int chain = n * H + h;
-    const WindowSpan sp = window_span(a, n, w, h == 0);
+    const WindowSpan sp = window_span(a, n, w, windowed ? a.wins : 1, h == 0);
     // A window pass that follows a chunk loop over other chains may start while that loop's
     // last chains still run; it ends only after them, so every later launch is ordered after
     // both (griddepcontrol.wait returns at once when nothing precedes the grid).
@@ -1187,7 +1195,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
             pdl_wait();
             const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
             const float *init = (w == 0) ? (a.init_state ? a.init_state + sbase : nullptr) : window_slot(a, lc, w, 0);
-            float *fin = (w == sp.wins_seq - 1 && a.final_state) ? a.final_state + sbase : nullptr;
+            // the last window ends the chain; window 0 of a windowed chain starts window 1
+            float *fin = (w == sp.wins_seq - 1) ? (a.final_state ? a.final_state + sbase : nullptr)
+                                                : (w == 0 ? window_slot(a, lc, 1, 0) : nullptr);
             const int chunk_base = sp.lw * w;
             state_loop(a, smem, B, tmem, n, h, bos, eos, nchunks, chunk_base, init, fin);
         }
@@ -1231,24 +1241,21 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     auto part = reinterpret_cast<float (*)[kCarryWarps][kCarryCols][kCarryRowPad]>(carry_dyn);
     const int blocks = kHeadDim / kCarryCols;
     const int lc = blockIdx.x / blocks;  // chain of this launch
-    const int pos = a.chain_base + lc;  // position in the launch order
+    const int pos = a.seq_chains + lc;  // position in the launch order
     const int c0 = (blockIdx.x - lc * blocks) * kCarryCols;
     pdl_launch_dependents();  // the output pass may start now; it waits for this grid on the device
     const int n = seq_of_rank(a, pos / a.num_heads, reinterpret_cast<int *>(carry_dyn));
     const int chain = n * a.num_heads + pos % a.num_heads;
-    const WindowSpan sp = window_span(a, n, 0, false);
-    if (sp.wins_seq <= 1) return;
+    (void)chain;
+    const WindowSpan sp = window_span(a, n, 0, a.wins, false);
+    if (sp.wins_seq <= 2) return;  // window 1's start state comes from window 0 itself
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const size_t sbase = (size_t)chain * kHeadDim * kHeadDim;
     const int k0 = 16 * warp;
     // warp w multiplies rows [k0, k0 + 16) of S and also reduces and rewrites exactly those
     // rows, so between window steps it waits only for its own lanes
     const int rr = k0 + (lane & 15), ch = lane >> 4;  // reduction: row rr, columns 4 ch .. 4 ch + 3
-    {
-        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (a.init_state) v = *reinterpret_cast<const float4 *>(a.init_state + sbase + (size_t)rr * kHeadDim + c0 + 4 * ch);
-        *reinterpret_cast<float4 *>(&S[rr][4 * ch]) = v;
-    }
+    *reinterpret_cast<float4 *>(&S[rr][4 * ch]) =
+        __ldcg(reinterpret_cast<const float4 *>(window_slot(a, lc, 1, 0) + (size_t)rr * kHeadDim + c0 + 4 * ch));
     float4 mv[16];  // M^T[k0 + kk][4 lane .. 4 lane + 3]
     auto map_row = [&](int w, int kk) {
         return reinterpret_cast<const float4 *>(window_slot(a, lc, w, 2) + (size_t)(k0 + kk) * kHeadDim + 4 * lane);
@@ -1257,10 +1264,10 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
         return __ldcg(reinterpret_cast<const float4 *>(window_slot(a, lc, w, 1) + (size_t)rr * kHeadDim + c0 + 4 * ch));
     };
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) mv[kk] = __ldcg(map_row(0, kk));
-    float4 e4 = load_e(0);
+    for (int kk = 0; kk < 16; ++kk) mv[kk] = __ldcg(map_row(1, kk));
+    float4 e4 = load_e(1);
     __syncwarp();
-    for (int w = 0; w + 1 < sp.wins_seq; ++w) {
+    for (int w = 1; w + 1 < sp.wins_seq; ++w) {
         const int b = w & 1;
         float acc[4][kCarryCols];
 #pragma unroll
@@ -1336,10 +1343,12 @@ WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_head
     // are unchanged. Each sequence's window length follows from its own length on the device.
     const int64_t tail = chains % sms;
     if (tail == 0 || tail * 3 > sms) return p;
-    const int64_t wins = std::min<int64_t>(sms / tail, max_chunks / kMinWindowChunks);
+    // window 0 of each chain runs beside the window pass of windows 1 .. wins - 2, and the
+    // output pass covers windows 1 .. wins - 1: wins - 1 CTAs per chain in each phase
+    const int64_t wins = std::min<int64_t>(sms / tail + 1, max_chunks / kMinWindowChunks);
     if (wins < 3) return p;
     p.wins = (int32_t)wins;
-    p.ws_bytes = tail * wins * kWindowSlotBytes;
+    p.ws_bytes = tail * window_slots(wins) * kStateBytes;
     p.seq_chains = (int32_t)(chains - tail);
     return p;
 }
@@ -1366,39 +1375,40 @@ cudaError_t launch_prefill_tc(const PrefillArgs &args, cudaStream_t stream) {
     cudaError_t e = configure_once<false>();
     if (e != cudaSuccess) return e;
     const int64_t all_chains = (int64_t)args.num_seqs * args.num_heads;
-    const int W = args.wins > 1 ? args.wins : 1;
-    // chains [0, seq) one CTA each, then chains [seq, all) on the window schedule
+    const int W = args.wins >= 3 ? args.wins : 1;
+    // positions [0, seq) run as whole chains, [seq, all) on the window schedule
     const int64_t seq = W == 1 ? all_chains : args.seq_chains;
-    if (seq > 0) {
-        PrefillArgs s = args;
-        s.wins = 1;
-        s.chain_base = 0;
-        kda_prefill_tc_kernel<false><<<(unsigned)seq, kThreadsTc, kSmemLaunch, stream>>>(s);
-        e = cudaGetLastError();
-        if (e != cudaSuccess || W == 1) return e;
-    }
-    PrefillArgs a = args;
-    a.chain_base = (int32_t)seq;
     const int64_t chains = all_chains - seq;
-    // Window schedule. Alone, the window pass waits for everything before it on the stream;
-    // after a chunk loop over other chains it may start in the SMs that loop's last chains
-    // leave free, and it ends after that loop. The carry follows the window pass; the output
-    // pass may start while the carry runs, its operand and solve warps working ahead while
-    // its state warps wait on the device for the carried start states.
+    PrefillArgs a = args;
+    a.wins = W;
+    a.seq_chains = (int32_t)seq;
+    // 1. The chunk loop: whole chains, then window 0 of each windowed chain, which leaves its
+    //    end state as window 1's start.
+    a.seq_ctas = (int32_t)seq;
+    a.win_first = 0;
+    a.win_count = 1;
+    kda_prefill_tc_kernel<false><<<(unsigned)(seq + chains), kThreadsTc, kSmemLaunch, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || W == 1) return e;
+    // 2. The window pass over windows 1 .. W - 2, a programmatic dependent of the chunk loop:
+    //    it fills the SMs as the loop's last CTAs start or leave, and waits for the loop before
+    //    it exits, so every later launch is ordered after both.
     e = configure_once<true>();
     if (e != cudaSuccess) return e;
-    const unsigned ctas = (unsigned)(chains * W);
-    if (seq > 0) {
-        e = launch_pdl(kda_prefill_tc_kernel<true>, ctas, kThreadsTc, kSmemLaunch, stream, a);
-    } else {
-        kda_prefill_tc_kernel<true><<<ctas, kThreadsTc, kSmemLaunch, stream>>>(a);
-        e = cudaGetLastError();
-    }
+    a.seq_ctas = 0;
+    a.win_first = 1;
+    a.win_count = W - 2;
+    e = launch_pdl(kda_prefill_tc_kernel<true>, (unsigned)(chains * (W - 2)), kThreadsTc, kSmemLaunch, stream, a);
     if (e != cudaSuccess) return e;
+    // 3. The carry: start states of windows 2 .. W - 1.
     kda_window_carry_kernel<<<(unsigned)(chains * (kHeadDim / kCarryCols)), kCarryThreads, kCarryDynSmem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_pdl(kda_prefill_tc_kernel<false>, ctas, kThreadsTc, kSmemLaunch, stream, a);
+    // 4. The output pass over windows 1 .. W - 1, a programmatic dependent of the carry: its
+    //    operand and solve warps work ahead while its state warps wait on the device for the
+    //    carried start states.
+    a.win_count = W - 1;
+    return launch_pdl(kda_prefill_tc_kernel<false>, (unsigned)(chains * (W - 1)), kThreadsTc, kSmemLaunch, stream, a);
 }
 
 }  // namespace kda

@@ -165,14 +165,14 @@ def test_product_path_has_no_fallback(monkeypatch, tmp_path):
 
 def test_window_plan_on_host(lib):
     """kda_prefill_workspace_size with an explicit SM count is host arithmetic only."""
-    slot = 3 * 128 * 128 * 4
-    assert K.kda_prefill_workspace_size(1, 8192, 8, sm_count=152) == 8 * 19 * slot   # 8 chains x 19 windows
-    assert K.kda_prefill_workspace_size(1, 512, 8, sm_count=152) == 8 * 4 * slot     # 16 chunks: 4 windows of 4
-    assert K.kda_prefill_workspace_size(16, 25729, 32, sm_count=152) == 0            # 512 chains fill the GPU
-    assert K.kda_prefill_workspace_size(8, 131072, 96, sm_count=152) == 8 * 19 * slot  # 5 full waves + 8 chains
-    assert K.kda_prefill_workspace_size(2, 8192, 76, sm_count=152) == 0              # exactly one full wave
-    assert K.kda_prefill_workspace_size(1, 8192, 204, sm_count=152) == 0             # 52-chain tail: > a third
-    assert K.kda_prefill_workspace_size(1, 8192, 202, sm_count=152) == 50 * 3 * slot # 50-chain tail, 3 windows
+    slot = 128 * 128 * 4  # one FP32 state; a chain with W windows keeps 3 W - 5 of them
+    assert K.kda_prefill_workspace_size(1, 8192, 8, sm_count=152) == 8 * 55 * slot    # 8 chains x 20 windows
+    assert K.kda_prefill_workspace_size(1, 512, 8, sm_count=152) == 8 * 7 * slot      # 16 chunks: 4 windows of 4
+    assert K.kda_prefill_workspace_size(16, 25729, 32, sm_count=152) == 0             # 512 chains fill the GPU
+    assert K.kda_prefill_workspace_size(8, 131072, 96, sm_count=152) == 8 * 55 * slot  # 5 full waves + 8 chains
+    assert K.kda_prefill_workspace_size(2, 8192, 76, sm_count=152) == 0               # exactly one full wave
+    assert K.kda_prefill_workspace_size(1, 8192, 204, sm_count=152) == 0              # 52-chain tail: > a third
+    assert K.kda_prefill_workspace_size(1, 8192, 202, sm_count=152) == 50 * 7 * slot  # 50-chain tail, 4 windows
     assert K.kda_prefill_workspace_size(1, 64, 1, sm_count=152) == 0                 # 2 chunks: no windows
     assert K.kda_prefill_workspace_size(0, 0, 1, sm_count=152) == 0
     with pytest.raises(K.KdaError):
