@@ -130,10 +130,11 @@ KDA_API int64_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_token
  * cut into windows that run in parallel; with more chains than multiprocessors, the
  * same is done for the chains of a last wave that holds at most a third of the GPU,
  * after the full waves have run one CTA per chain. This follows the windowed "affine
- * composite" of FlashInfer PR #5573 ("1. Composite schedule"): a window pass computes,
- * from a zero start, each window's end state E and linear map M (S_end = M S_start + E);
- * an FP32 carry pass walks the windows of each chain; the output pass then reruns every
- * window from its true start state. Results match kda_prefill up to rounding.
+ * composite" of FlashInfer PR #5573 ("1. Composite schedule"): window 0 runs from the
+ * initial state; beside it a window pass computes, from a zero start, each later window's
+ * end state E and linear map M (S_end = M S_start + E); an FP32 carry pass walks the
+ * windows of each chain; the output pass then reruns windows 1 onwards from their true
+ * start states. Results match kda_prefill up to rounding.
  *   checkpoints      FP32 [ckpt_rows, num_heads, 128, 128] intermediate states, or NULL with
  *                    ckpt_every = 0 (the FP32 checkpoint rows every 64 tokens of FlashInfer PR
  *                    #5565, "1. Kernel body"): with ckpt_every > 0 (a multiple of 32), the state
