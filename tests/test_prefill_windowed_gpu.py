@@ -139,3 +139,39 @@ def test_windowed_tail_after_full_waves():
     assert_out_close(out[:, heads], ref_out)
     assert_state_close(fin[:, heads], ref_fin)
     assert tail == H - first
+
+
+def test_windowed_three_windows_minimum():
+    """13 chunks on 2 chains: the smallest plan, windows 0, 1 and 2 of 5, 5 and 3 chunks
+    (window 0 from the initial state, one window pass, one carry step)."""
+    assert K.kda_prefill_workspace_size(1, 400, 2, sm_count=152) == 2 * 4 * 128 * 128 * 4
+    inp = S.prefill_inputs([400], 2, seed=36, init_std=0.02)
+    check(inp, lower_bound=-5.0, gate_mode="lower_bound")
+
+
+def test_windowed_tail_of_a_varlen_batch():
+    """39 sequences x 4 heads = 156 chains: the 4 chains of the shortest sequence, which
+    start last, take the window schedule after the full wave; the full wave matches the
+    chunk loop bitwise and the windowed chains match the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 4
+    N = sms // H + 1
+    gen = torch.Generator().manual_seed(37)
+    lens = (torch.randint(700, 1400, (N,), generator=gen)).tolist()
+    lens[N // 2] = 520  # the shortest: 17 chunks in windows of at least 4
+    inp = S.prefill_inputs(lens, H, seed=37, init_std=0.02)
+    assert K.kda_prefill_workspace_size(N, sum(lens), H) > 0
+    out, fin = windowed(inp, lower_bound=-5.0, gate_mode="lower_bound")
+    d = to_dev(inp)
+    out_s, fin_s = K.prefill(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], d["cu_seqlens"], d["init_state"],
+                             scale=SCALE, lower_bound=-5.0)
+    cu = inp["cu_seqlens"].tolist()
+    short = N // 2
+    others = [n for n in range(N) if n != short]
+    for n in others:
+        sl = slice(cu[n], cu[n + 1])
+        assert torch.equal(out[sl], out_s[sl].cpu()) and torch.equal(fin[n], fin_s[n].cpu()), n
+    sub = slice_problem(inp, seqs=[short, others[0], others[-1]])
+    ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=-5.0, gate_mode="lower_bound")
+    assert_out_close(out[sub["token_index"]], ref_out)
+    assert_state_close(fin[[short, others[0], others[-1]]], ref_fin)
