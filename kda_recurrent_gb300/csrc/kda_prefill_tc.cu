@@ -1147,7 +1147,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     // last chains still run; it ends only after them, so every later launch is ordered after
     // both (griddepcontrol.wait returns at once when nothing precedes the grid).
     if (!kPass1) pdl_launch_dependents();
-    // The window pass covers every window but the last (its map is never needed).
+    // The window pass covers every window but the first (which starts from the initial state)
+    // and the last (whose map is never needed); the output pass, every window that exists.
     if (kPass1 ? (w >= sp.wins_seq - 1) : !sp.live) {
         if (kPass1) pdl_wait();
         return;
