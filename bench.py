@@ -59,6 +59,11 @@ def parse_args(argv=None):
                    help="comma-separated sequence lengths replacing the prefill workload's (small ncu cases)")
     p.add_argument("--heads", type=int, default=None, help="head count replacing the prefill workload's")
     p.add_argument("--pool-slots", type=int, default=None, help="decode pool size replacing 16384 (small ncu cases)")
+    p.add_argument("--decode-tokens", type=int, default=1,
+                   help="tokens per decode row (kda_decode_ex, up to 16); above 1 the e2e and CPU legs are skipped")
+    p.add_argument("--ckpt-every", type=int, default=0,
+                   help="prefill also writes the FP32 state every N tokens (a multiple of 32) as checkpoints; "
+                        "the e2e and CPU legs are then skipped")
     p.add_argument("--no-windows", action="store_true",
                    help="run kda_prefill (sequential chunk loop) instead of kda_prefill_ex with a workspace")
     return p.parse_args(argv)
@@ -179,7 +184,7 @@ def prefill_workload(name, device, seed_offset=0, seqlens=None, heads=None):
     return cfg, inp
 
 
-def decode_workload(rows, state_dtype, device, seed_offset=0, pool_slots=None):
+def decode_workload(rows, state_dtype, device, seed_offset=0, pool_slots=None, tokens=1):
     import dataclasses
 
     import kda_synth as S
@@ -188,7 +193,9 @@ def decode_workload(rows, state_dtype, device, seed_offset=0, pool_slots=None):
         cfg = dataclasses.replace(cfg, num_slots=pool_slots)
     seed = rank_seed(cfg.seed, seed_offset)
     pool = S.state_pool(cfg.num_slots, cfg.num_heads, state_dtype, std=cfg.pool_std, seed=seed, device=device)
-    inp = S.decode_inputs(rows, cfg.num_heads, seed=seed, device=device)
+    inp = S.decode_inputs(rows * tokens, cfg.num_heads, seed=seed, device=device)
+    if tokens > 1:  # [rows, tokens, H, 128] and [rows, tokens, H]
+        inp = {k: v.view(rows, tokens, *v.shape[1:]) for k, v in inp.items()}
     inp["slot_idx"] = S.slot_indices(rows, cfg.num_slots, seed=seed, device=device)
     return cfg, pool, inp
 
@@ -203,9 +210,9 @@ def prefill_bytes(cfg):
     return prefill_units(cfg) * PREFILL_BYTES_PER_TOKEN_HEAD + state_io
 
 
-def decode_bytes(rows, heads, state_dtype):
+def decode_bytes(rows, heads, state_dtype, tokens=1):
     per_state = 128 * 128 * (4 if state_dtype == "f32" else 2)
-    return rows * heads * (2 * per_state + DECODE_IO_BYTES_PER_ROW_HEAD) + rows * 4
+    return rows * heads * (2 * per_state + tokens * DECODE_IO_BYTES_PER_ROW_HEAD) + rows * 4
 
 
 # ------------------------------------------------------------------ our arm
@@ -224,7 +231,12 @@ def run_ours(args):
 
     seqlens = [int(x) for x in args.seqlens.split(",")] if args.seqlens else None
     pcfg, pin = prefill_workload(args.prefill, device, rank, seqlens, args.heads)
-    dcfg, pool, din = decode_workload(args.decode_rows, args.state_dtype, device, rank, args.pool_slots)
+    T = args.decode_tokens
+    if not 1 <= T <= 16:
+        raise SystemExit("--decode-tokens takes 1 .. 16")
+    if T > 1 or args.ckpt_every:  # the e2e and CPU legs time the plain calls
+        args.no_e2e = args.no_cpu_baseline = True
+    dcfg, pool, din = decode_workload(args.decode_rows, args.state_dtype, device, rank, args.pool_slots, T)
     scale = pcfg.scale
     out = torch.empty_like(pin["q"])
     fin = torch.empty(len(pcfg.seqlens), pcfg.num_heads, 128, 128, dtype=torch.float32, device=device)
@@ -240,13 +252,28 @@ def run_ours(args):
     # chunk loop (full waves and window 0) + window pass + carry + output pass, or the chunk loop
     prefill_launches = 4 if ws is not None else 1
 
+    ck = ck_off = None
+    ck_rows = 0
+    if args.ckpt_every:
+        if args.ckpt_every % 32:
+            raise SystemExit("--ckpt-every takes a multiple of 32")
+        per_seq = [n // args.ckpt_every for n in pcfg.seqlens]
+        ck_rows = sum(per_seq)
+        ck = torch.empty(max(ck_rows, 1), pcfg.num_heads, 128, 128, dtype=torch.float32, device=device)
+        ck_off = torch.tensor([sum(per_seq[:i]) for i in range(len(per_seq))], dtype=torch.int32, device=device)
+
     def prefill_call():
         K.kda_prefill_ex(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta"], pin["cu_seqlens"],
-                         pin["init_state"], out, fin, scale, pcfg.lower_bound, pcfg.gate_mode, ws, stream)
+                         pin["init_state"], out, fin, scale, pcfg.lower_bound, pcfg.gate_mode, ws, stream,
+                         checkpoints=ck, ckpt_offsets=ck_off, ckpt_every=args.ckpt_every)
 
     def decode_call():
-        K.kda_decode(din["q"], din["k"], din["v"], din["g_raw"], din["beta"], din["slot_idx"], pool, dout, dcfg.scale,
-                     dcfg.lower_bound, dcfg.gate_mode, stream)
+        if T == 1:
+            K.kda_decode(din["q"], din["k"], din["v"], din["g_raw"], din["beta"], din["slot_idx"], pool, dout,
+                         dcfg.scale, dcfg.lower_bound, dcfg.gate_mode, stream)
+        else:
+            K.kda_decode_ex(din["q"], din["k"], din["v"], din["g_raw"], din["beta"], din["slot_idx"], pool, dout,
+                            dcfg.scale, dcfg.lower_bound, dcfg.gate_mode, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -297,11 +324,11 @@ def run_ours(args):
         return None
 
     p_units = prefill_units(pcfg) * world
-    d_units = args.decode_rows * dcfg.num_heads * world
+    d_units = args.decode_rows * dcfg.num_heads * T * world  # (row, head) items x tokens
     p_rate = p_units / (p_mean * 1e-3)
     d_rate = d_units / (d_mean * 1e-3)
-    p_bytes = prefill_bytes(pcfg)
-    d_bytes = decode_bytes(args.decode_rows, dcfg.num_heads, args.state_dtype)
+    p_bytes = prefill_bytes(pcfg) + ck_rows * pcfg.num_heads * STATE_BYTES
+    d_bytes = decode_bytes(args.decode_rows, dcfg.num_heads, args.state_dtype, T)
     p_gbs = p_bytes / (p_mean * 1e-3) / 1e9
     d_gbs = d_bytes / (d_mean * 1e-3) / 1e9
     p_tflops = prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD / (p_mean * 1e-3) / 1e12
@@ -311,7 +338,7 @@ def run_ours(args):
     prefill_roof = {"bound": "hbm", "achieved": round(p_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(p_gbs / peaks["hbm_gbs"], 5),
                     "traffic": (scaled_traffic(traffic, "kda_prefill_tc_kernel", prefill_units(pcfg))
-                                if ws is None else None),
+                                if ws is None and not ck_rows else None),
                     "kernel": ("kda_prefill_tc_kernel" if ws is None else
                                ("kda_prefill_tc_kernel full waves + " if full_waves else "") +
                                "kda_prefill_ex window schedule (window 0, window pass, carry, output pass)"), "peak_source": peak_src,
@@ -319,11 +346,12 @@ def run_ours(args):
                     "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": round(p_tflops / peaks["bf16_tflops"], 5),
                                "flop_per_launch": prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD}}
-    d_kernel = decode_kernel_name(args.decode_rows * dcfg.num_heads, sms, args.state_dtype)
+    d_kernel = (decode_kernel_name(args.decode_rows * dcfg.num_heads, sms, args.state_dtype) if T == 1
+                else "kda_decode_stream_kernel")
     decode_roof = {"bound": "hbm", "achieved": round(d_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                    "frac": round(d_gbs / peaks["hbm_gbs"], 5),
-                   "traffic": scaled_traffic(traffic, f"{d_kernel}<{args.state_dtype}>",
-                                             args.decode_rows * dcfg.num_heads),
+                   "traffic": (scaled_traffic(traffic, f"{d_kernel}<{args.state_dtype}>",
+                                              args.decode_rows * dcfg.num_heads) if T == 1 else None),
                    "kernel": d_kernel, "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes}
     dominant = prefill_roof if p_mean >= d_mean else decode_roof
     line = {
@@ -334,9 +362,9 @@ def run_ours(args):
         "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool{dcfg.num_slots}",
                    "prefill": {"seqlens": pcfg.seqlens if len(pcfg.seqlens) <= 16 else f"{len(pcfg.seqlens)} seqs",
                                "heads": pcfg.num_heads, "gate": pcfg.gate_mode, "lower_bound": pcfg.lower_bound,
-                               "init_state": pcfg.init_std is not None},
+                               "init_state": pcfg.init_std is not None, "ckpt_every": args.ckpt_every},
                    "decode": {"rows": args.decode_rows, "heads": dcfg.num_heads, "pool_slots": dcfg.num_slots,
-                              "state_dtype": args.state_dtype},
+                              "state_dtype": args.state_dtype, "tokens_per_row": T},
                    "precision": "bf16 operands, tf32 state update, fp32 state and accumulation",
                    "prefill_schedule": ("sequential chunk loop" if ws is None else
                                         (f"{full_waves} full waves of the chunk loop, then "
@@ -347,7 +375,8 @@ def run_ours(args):
         "prefill": {"value": round(p_rate, 1), "unit": "tokens*heads/s", "ms": round(p_mean, 4),
                     "us_per_chunk_per_chain": round(p_mean * 1e3 / (math.ceil(max(pcfg.seqlens) / 32) * waves), 4),
                     "waves": waves},
-        "decode": {"value": round(d_rate, 1), "unit": "rows*heads/s", "ms": round(d_mean, 4), "roofline": decode_roof},
+        "decode": {"value": round(d_rate, 1), "unit": "rows*heads/s" if T == 1 else "tokens*heads/s",
+                   "ms": round(d_mean, 4), "roofline": decode_roof},
         "roofline": dominant,
         "roofline_prefill": prefill_roof,
         "gpu_launches": (prefill_launches + 1) * args.steps,
