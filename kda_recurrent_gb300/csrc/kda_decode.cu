@@ -264,18 +264,23 @@ struct StreamShape {
     static constexpr bool kGroups = sizeof(T) == 2;
     static constexpr int kGroupBytes = 2 * 8 * kHeadDim * 4 + 4 * kHeadDim * 4 + kMaxTokensPerRow * 4;
     static constexpr int kRed = 2 * RPP * kHeadDim * 4;
-    static constexpr int kFixed = (kGroups ? 2 * kGroupBytes : kRed + 4 * kHeadDim * 4 + kMaxTokensPerRow * 4) +
-                                  2 * kMaxStages * 8;
-    static constexpr int kStreamSmem = 220 * 1024;
+    // FP32 states: the partial sums, u and beta, then the decay, k and q vectors of every
+    // token of the item ([tokens][3][128], filled once per item); the mbarriers last
+    static constexpr int kScalars = kRed + kHeadDim * 4 + kMaxTokensPerRow * 4;
+    static constexpr int kBarBytes = 2 * kMaxStages * 8;
+    static __host__ __device__ int fixed(int tokens) {
+        return (kGroups ? 2 * kGroupBytes : kScalars + 3 * tokens * kHeadDim * 4) + kBarBytes;
+    }
+    static constexpr int kStreamSmem = 227 * 1024;
     static __host__ __device__ uint32_t stage_bytes(int tokens) { return kItemBytes + kTokBytes * tokens; }
     static __host__ __device__ int stages(int tokens) {
-        const int n = (int)((kStreamSmem - kFixed) / stage_bytes(tokens));
+        const int n = (int)((kStreamSmem - fixed(tokens)) / stage_bytes(tokens));
         // consecutive fills of a stage are NS items apart; with two compute groups taking
         // alternate items, an even NS gives both fills to the same group, which waits for the
         // earlier fill's phase before it can wait for the later one
         return kGroups ? (n < kMaxStages ? n : kMaxStages) & ~1 : (n < kMaxStages ? n : kMaxStages);
     }
-    static __host__ __device__ int smem(int tokens) { return stages(tokens) * stage_bytes(tokens) + kFixed; }
+    static __host__ __device__ int smem(int tokens) { return stages(tokens) * stage_bytes(tokens) + fixed(tokens); }
 };
 
 __device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kDecodeThreads) : "memory"); }
@@ -454,12 +459,10 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *const stages = smem;
     float *const s_red = reinterpret_cast<float *>(smem + NS * stage_bytes);  // [2][RPP][128]
-    float *const s_k = s_red + 2 * RPP * kHeadDim;
-    float *const s_q = s_k + kHeadDim;
-    float *const s_decay = s_q + kHeadDim;
-    float *const s_u = s_decay + kHeadDim;
-    float *const s_beta = s_u + kHeadDim;  // [kMaxTokensPerRow]
-    uint64_t *const full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes + SS::kFixed - 2 * SS::kMaxStages * 8);
+    float *const s_u = s_red + 2 * RPP * kHeadDim;
+    float *const s_beta = s_u + kHeadDim;        // [kMaxTokensPerRow]
+    float *const s_vec = s_beta + kMaxTokensPerRow;  // [TT][decay, k, q][128]
+    uint64_t *const full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes + SS::fixed(TT) - SS::kBarBytes);
     uint64_t *const done = full + SS::kMaxStages;
 
     const int tid = threadIdx.x;
@@ -583,19 +586,26 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                 *reinterpret_cast<const typename V::Raw *>(S + (rg + p * RPP) * kHeadDim + cg * VEC);
             V::unpack(raw, stv[p]);
         }
+        // the decay, k and q vectors of all the item's tokens at once, so that each token
+        // step needs only the two barriers around its column sums
+        const __nv_bfloat16 *const rows0 =
+            reinterpret_cast<const __nv_bfloat16 *>(stages + (size_t)st * stage_bytes + SS::kItemBytes);
+        compute_bar();  // the previous item's use of the shared vectors is over
+        for (int x = tid; x < TT * kHeadDim; x += kDecodeThreads) {
+            const int t = x >> 7, c = x & (kHeadDim - 1);
+            const __nv_bfloat16 *trow = rows0 + t * (SS::kTokBytes / 2);
+            float *const v3 = s_vec + t * 3 * kHeadDim;
+            v3[c] = expf(gate_log_decay(__bfloat162float(trow[2 * kHeadDim + c]), a.gate_mode, a.lower_bound));
+            v3[kHeadDim + c] = __bfloat162float(trow[kHeadDim + c]);
+            v3[2 * kHeadDim + c] = __bfloat162float(trow[c]);
+        }
+        if (tid < TT) s_beta[tid] = beta_mine;
+        compute_bar();
         for (int t = 0; t < TT; ++t) {
-            const __nv_bfloat16 *trow =
-                reinterpret_cast<const __nv_bfloat16 *>(stages + (size_t)st * stage_bytes + SS::kItemBytes +
-                                                        t * SS::kTokBytes);
-            compute_bar();  // the previous step's use of the shared vectors is over
-            if (tid < kHeadDim) {
-                const float av = __bfloat162float(trow[2 * kHeadDim + tid]);
-                s_decay[tid] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
-                s_k[tid] = __bfloat162float(trow[kHeadDim + tid]);
-                s_q[tid] = __bfloat162float(trow[tid]);
-            }
-            if (t == 0 && tid < TT) s_beta[tid] = beta_mine;
-            compute_bar();
+            const __nv_bfloat16 *trow = rows0 + t * (SS::kTokBytes / 2);
+            const float *const s_decay = s_vec + t * 3 * kHeadDim;
+            const float *const s_k = s_decay + kHeadDim;
+            const float *const s_q = s_k + kHeadDim;
             const TokenScalars ts = token_scalars(s_q, s_k, a);
             float wk[VEC], wq[VEC];
 #pragma unroll
@@ -636,6 +646,8 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) stv[p][e] = fmaf(kr, s_u[cg * VEC + e], stv[p][e]);
             }
+            // the next token's partial sums overwrite s_red only after this token's column
+            // sums were read (the barrier above), and s_u only after the next barrier
         }
 #pragma unroll
         for (int p = 0; p < NPASS; ++p)
