@@ -607,24 +607,30 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             const float *const s_k = s_decay + kHeadDim;
             const float *const s_q = s_k + kHeadDim;
             const TokenScalars ts = token_scalars(s_q, s_k, a);
-            float wk[VEC], wq[VEC];
+            // packed FP32 pairs of columns (one instruction for two lanes of the pair)
+            float2 wk[VEC / 2], wq[VEC / 2];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) wk[e] = wq[e] = 0.0f;
+            for (int e = 0; e < VEC / 2; ++e) wk[e] = wq[e] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int p = 0; p < NPASS; ++p) {
                 const int row = rg + p * RPP;
-                const float d = s_decay[row], kr = s_k[row], qr = s_q[row];
+                const float2 d = make_float2(s_decay[row], s_decay[row]);
+                const float2 kr = make_float2(s_k[row], s_k[row]), qr = make_float2(s_q[row], s_q[row]);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    stv[p][e] *= d;
-                    wk[e] = fmaf(stv[p][e], kr, wk[e]);
-                    wq[e] = fmaf(stv[p][e], qr, wq[e]);
+                for (int e = 0; e < VEC / 2; ++e) {
+                    const float2 y = __fmul2_rn(make_float2(stv[p][2 * e], stv[p][2 * e + 1]), d);
+                    stv[p][2 * e] = y.x;
+                    stv[p][2 * e + 1] = y.y;
+                    wk[e] = __ffma2_rn(y, kr, wk[e]);
+                    wq[e] = __ffma2_rn(y, qr, wq[e]);
                 }
             }
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                s_red[(0 * RPP + rg) * kHeadDim + cg * VEC + e] = wk[e] * ts.rk;
-                s_red[(1 * RPP + rg) * kHeadDim + cg * VEC + e] = wq[e] * ts.rq;
+            for (int e = 0; e < VEC / 2; ++e) {
+                *reinterpret_cast<float2 *>(&s_red[(0 * RPP + rg) * kHeadDim + cg * VEC + 2 * e]) =
+                    __fmul2_rn(wk[e], make_float2(ts.rk, ts.rk));
+                *reinterpret_cast<float2 *>(&s_red[(1 * RPP + rg) * kHeadDim + cg * VEC + 2 * e]) =
+                    __fmul2_rn(wq[e], make_float2(ts.rq, ts.rq));
             }
             compute_bar();
             if (tid < kHeadDim) {
@@ -639,12 +645,19 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                 a.out[tok_index(item, t) * kHeadDim + tid] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
             }
             compute_bar();
+            float2 uv[VEC / 2];
+#pragma unroll
+            for (int e = 0; e < VEC / 2; ++e) uv[e] = *reinterpret_cast<const float2 *>(&s_u[cg * VEC + 2 * e]);
 #pragma unroll
             for (int p = 0; p < NPASS; ++p) {
                 const int row = rg + p * RPP;
                 const float kr = s_k[row] * ts.rk;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) stv[p][e] = fmaf(kr, s_u[cg * VEC + e], stv[p][e]);
+                for (int e = 0; e < VEC / 2; ++e) {
+                    const float2 x = __ffma2_rn(make_float2(kr, kr), uv[e], make_float2(stv[p][2 * e], stv[p][2 * e + 1]));
+                    stv[p][2 * e] = x.x;
+                    stv[p][2 * e + 1] = x.y;
+                }
             }
             // the next token's partial sums overwrite s_red only after this token's column
             // sums were read (the barrier above), and s_u only after the next barrier
