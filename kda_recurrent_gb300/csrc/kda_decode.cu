@@ -92,12 +92,13 @@ struct TokenScalars {
 // Every calling warp computes q.k and, when the call asks for it, the L2 normalisation
 // factors (sum x^2 + eps)^-1/2 of q and k from the token vectors in shared memory; each
 // warp reads the same 2 x 128 values, so no barrier is needed.
-__device__ __forceinline__ TokenScalars token_scalars(const float *s_q, const float *s_k, const DecodeArgs &a) {
+template <typename E>
+__device__ __forceinline__ TokenScalars token_scalars(const E *s_q, const E *s_k, const DecodeArgs &a) {
     const int lane = threadIdx.x & 31;
     float qk = 0.0f, qq = 0.0f, kk = 0.0f;
 #pragma unroll
     for (int i = lane; i < kHeadDim; i += 32) {
-        const float q = s_q[i], k = s_k[i];
+        const float q = static_cast<float>(s_q[i]), k = static_cast<float>(s_k[i]);
         qk = fmaf(q, k, qk);
         qq = fmaf(q, q, qq);
         kk = fmaf(k, k, kk);
@@ -266,7 +267,7 @@ struct StreamShape {
     static constexpr int kRed = 2 * RPP * kHeadDim * 4;
     // FP32 states: the partial sums, u and beta, then the decay, k and q vectors of every
     // token of the item ([tokens][3][128], filled once per item); the mbarriers last
-    static constexpr int kScalars = kRed + kHeadDim * 4 + kMaxTokensPerRow * 4;
+    static constexpr int kScalars = kRed + kHeadDim * 4 + kMaxTokensPerRow * 4 + kMaxTokensPerRow * 16;
     static constexpr int kBarBytes = 2 * kMaxStages * 8;
     static __host__ __device__ int fixed(int tokens) {
         return (kGroups ? 2 * kGroupBytes : kScalars + 3 * tokens * kHeadDim * 4) + kBarBytes;
@@ -461,7 +462,8 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     float *const s_red = reinterpret_cast<float *>(smem + NS * stage_bytes);  // [2][RPP][128]
     float *const s_u = s_red + 2 * RPP * kHeadDim;
     float *const s_beta = s_u + kHeadDim;        // [kMaxTokensPerRow]
-    float *const s_vec = s_beta + kMaxTokensPerRow;  // [TT][decay, k, q][128]
+    float4 *const s_ts = reinterpret_cast<float4 *>(s_beta + kMaxTokensPerRow);  // [kMaxTokensPerRow] (qk, rq, rk)
+    float *const s_vec = reinterpret_cast<float *>(s_ts + kMaxTokensPerRow);     // [TT][decay, k, q][128]
     uint64_t *const full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes + SS::fixed(TT) - SS::kBarBytes);
     uint64_t *const done = full + SS::kMaxStages;
 
@@ -600,13 +602,23 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             v3[2 * kHeadDim + c] = __bfloat162float(trow[c]);
         }
         if (tid < TT) s_beta[tid] = beta_mine;
+        // q.k and the normalisation factors of token t by warp t mod 8, from the token rows
+        for (int t = tid >> 5; t < TT; t += kDecodeThreads / 32) {
+            const __nv_bfloat16 *trow = rows0 + t * (SS::kTokBytes / 2);
+            const TokenScalars x = token_scalars(trow, trow + kHeadDim, a);
+            if ((tid & 31) == 0) s_ts[t] = make_float4(x.qk, x.rq, x.rk, 0.0f);
+        }
         compute_bar();
         for (int t = 0; t < TT; ++t) {
             const __nv_bfloat16 *trow = rows0 + t * (SS::kTokBytes / 2);
             const float *const s_decay = s_vec + t * 3 * kHeadDim;
             const float *const s_k = s_decay + kHeadDim;
             const float *const s_q = s_k + kHeadDim;
-            const TokenScalars ts = token_scalars(s_q, s_k, a);
+            TokenScalars ts;
+            {
+                const float4 x = s_ts[t];
+                ts.qk = x.x, ts.rq = x.y, ts.rk = x.z;
+            }
             // packed FP32 pairs of columns (one instruction for two lanes of the pair)
             float2 wk[VEC / 2], wq[VEC / 2];
 #pragma unroll
