@@ -6,8 +6,9 @@
 * the anchor-cancellation identity 2^(G_i - C) 2^(C - G_j) = 2^(G_i - G_j) and the
   range of the anchored operands;
 * closed forms: beta = 0; beta = 0 with g = 0; the delta-rule write at beta = 1;
-* invariants: linearity in (S0, V), split at any token, varlen = separate sequences,
-  dk-channel permutation, decode = prefill of length one;
+* invariants: linearity in (S0, V), split at any token, the window affine composite
+  S_end = M S_start + E, varlen = separate sequences, dk-channel permutation, decode =
+  prefill of length one;
 * the gate against library routines, and a two-token d = 2 example worked by hand;
 * planted mistakes (a dropped decay, a transposed read-out, a misplaced beta, a wrong
   prefix) that at least one pin must reject.
@@ -216,6 +217,28 @@ def test_split_and_carry_is_bitwise(cut):
                                f1, scale=0.3, lower_bound=-5.0)
     assert np.array_equal(np.concatenate([o1, o2]), out)
     assert np.array_equal(f2, fin)
+
+
+@pytest.mark.parametrize("mode,lb", [("lower_bound", -5.0), ("softplus", 0.0)])
+def test_window_affine_composite(mode, lb):
+    """The window schedule's reading of the composite schedule of FlashInfer PR #5573
+    ("1. Composite schedule"): over a window, S_end = M S_start + E, where E is the window
+    run from a zero state and M the window run from S_start = I with V = 0 (d_k = d_v), and
+    the window's outputs are the zero-start outputs plus those of the V = 0 run from S_start."""
+    d = 16
+    c = make_case(150, 1, d, d, seed=12, mode=mode)
+    cut = 64
+    out, fin, _ = run(c, mode, lb)
+    part = lambda x: x[cut:]
+    win = dict(q=part(c["q"]), k=part(c["k"]), v=part(c["v"]), a=part(c["a"]), beta=part(c["beta"]),
+               cu=np.array([0, 150 - cut], dtype=np.int32))
+    _, s_start, _ = oracle.prefill(c["q"][:cut], c["k"][:cut], c["v"][:cut], c["a"][:cut], c["beta"][:cut],
+                                   np.array([0, cut]), c["s0"], scale=0.3, lower_bound=lb, gate_mode=mode)
+    o_e, e, _ = run(dict(win, s0=np.zeros((1, 1, d, d))), mode, lb)
+    _, m, _ = run(dict(win, v=np.zeros_like(win["v"]), s0=np.eye(d)[None, None]), mode, lb)
+    o_s, _, _ = run(dict(win, v=np.zeros_like(win["v"]), s0=s_start), mode, lb)
+    assert rel(m[0, 0] @ s_start[0, 0] + e[0, 0], fin[0, 0]) < 1e-12
+    assert rel(o_e + o_s, out[cut:]) < 1e-12
 
 
 def test_varlen_equals_separate_sequences_bitwise():
