@@ -589,17 +589,19 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             V::unpack(raw, stv[p]);
         }
         // the decay, k and q vectors of all the item's tokens at once, so that each token
-        // step needs only the two barriers around its column sums
+        // step needs only the two barriers around its column sums. Channel c is stored at
+        // (c mod RPP) NPASS + c / RPP, so that the NPASS rows a thread owns are contiguous.
         const __nv_bfloat16 *const rows0 =
             reinterpret_cast<const __nv_bfloat16 *>(stages + (size_t)st * stage_bytes + SS::kItemBytes);
         compute_bar();  // the previous item's use of the shared vectors is over
         for (int x = tid; x < TT * kHeadDim; x += kDecodeThreads) {
             const int t = x >> 7, c = x & (kHeadDim - 1);
+            const int pc = (c % RPP) * NPASS + c / RPP;
             const __nv_bfloat16 *trow = rows0 + t * (SS::kTokBytes / 2);
             float *const v3 = s_vec + t * 3 * kHeadDim;
-            v3[c] = expf(gate_log_decay(__bfloat162float(trow[2 * kHeadDim + c]), a.gate_mode, a.lower_bound));
-            v3[kHeadDim + c] = __bfloat162float(trow[kHeadDim + c]);
-            v3[2 * kHeadDim + c] = __bfloat162float(trow[c]);
+            v3[pc] = expf(gate_log_decay(__bfloat162float(trow[2 * kHeadDim + c]), a.gate_mode, a.lower_bound));
+            v3[kHeadDim + pc] = __bfloat162float(trow[kHeadDim + c]);
+            v3[2 * kHeadDim + pc] = __bfloat162float(trow[c]);
         }
         if (tid < TT) s_beta[tid] = beta_mine;
         // q.k and the normalisation factors of token t by warp t mod 8, from the token rows
@@ -619,15 +621,25 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                 const float4 x = s_ts[t];
                 ts.qk = x.x, ts.rq = x.y, ts.rk = x.z;
             }
+            // this thread's rows rg + p RPP of the decay, k and q vectors, 16 bytes at a time
+            float dv[NPASS], kv[NPASS], qv[NPASS];
+#pragma unroll
+            for (int p4 = 0; p4 < NPASS / 4; ++p4) {
+                const float4 d4 = reinterpret_cast<const float4 *>(s_decay + rg * NPASS)[p4];
+                const float4 k4 = reinterpret_cast<const float4 *>(s_k + rg * NPASS)[p4];
+                const float4 q4 = reinterpret_cast<const float4 *>(s_q + rg * NPASS)[p4];
+                dv[4 * p4] = d4.x, dv[4 * p4 + 1] = d4.y, dv[4 * p4 + 2] = d4.z, dv[4 * p4 + 3] = d4.w;
+                kv[4 * p4] = k4.x, kv[4 * p4 + 1] = k4.y, kv[4 * p4 + 2] = k4.z, kv[4 * p4 + 3] = k4.w;
+                qv[4 * p4] = q4.x, qv[4 * p4 + 1] = q4.y, qv[4 * p4 + 2] = q4.z, qv[4 * p4 + 3] = q4.w;
+            }
             // packed FP32 pairs of columns (one instruction for two lanes of the pair)
             float2 wk[VEC / 2], wq[VEC / 2];
 #pragma unroll
             for (int e = 0; e < VEC / 2; ++e) wk[e] = wq[e] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int p = 0; p < NPASS; ++p) {
-                const int row = rg + p * RPP;
-                const float2 d = make_float2(s_decay[row], s_decay[row]);
-                const float2 kr = make_float2(s_k[row], s_k[row]), qr = make_float2(s_q[row], s_q[row]);
+                const float2 d = make_float2(dv[p], dv[p]);
+                const float2 kr = make_float2(kv[p], kv[p]), qr = make_float2(qv[p], qv[p]);
 #pragma unroll
                 for (int e = 0; e < VEC / 2; ++e) {
                     const float2 y = __fmul2_rn(make_float2(stv[p][2 * e], stv[p][2 * e + 1]), d);
@@ -662,8 +674,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             for (int e = 0; e < VEC / 2; ++e) uv[e] = *reinterpret_cast<const float2 *>(&s_u[cg * VEC + 2 * e]);
 #pragma unroll
             for (int p = 0; p < NPASS; ++p) {
-                const int row = rg + p * RPP;
-                const float kr = s_k[row] * ts.rk;
+                const float kr = kv[p] * ts.rk;
 #pragma unroll
                 for (int e = 0; e < VEC / 2; ++e) {
                     const float2 x = __ffma2_rn(make_float2(kr, kr), uv[e], make_float2(stv[p][2 * e], stv[p][2 * e + 1]));
