@@ -242,7 +242,6 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_but_newest() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -539,18 +538,11 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                     bulk_store(dst + p, smem_addr(stages + (size_t)st * stage_bytes + p), SS::kPiece);
             }
             bulk_commit();  // one group per item, empty for a skipped one
-            if (NS >= 3) {
-                // the stage of the previous item is refilled once its store has read it,
-                // which has had this item's wait to happen in
-                if (j >= 1 && j - 1 + NS < mine) {
-                    bulk_wait_read_but_newest();
-                    issue(j - 1 + NS);
-                }
-            } else if (j + NS < mine) {
-                // with two stages that refill would come too late: the next item must stream
-                // in while this one is computed, so this stage is refilled at once
-                bulk_wait_read_all();
-                issue(j + NS);
+            // the stage of the previous item is refilled once its store has read it, which
+            // has had this item's wait to happen in
+            if (j >= 1 && j - 1 + NS < mine) {
+                bulk_wait_read_but_newest();
+                issue(j - 1 + NS);
             }
         }
         bulk_wait_all();
