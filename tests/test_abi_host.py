@@ -174,6 +174,11 @@ def test_window_plan_on_host(lib):
     assert K.kda_prefill_workspace_size(1, 8192, 204, sm_count=152) == 0              # 52-chain tail: > a third
     assert K.kda_prefill_workspace_size(1, 8192, 202, sm_count=152) == 50 * 7 * slot  # 50-chain tail, 4 windows
     assert K.kda_prefill_workspace_size(1, 64, 1, sm_count=152) == 0                 # 2 chunks: no windows
+    # a small GPU: W = min(SMs / tail + 1, chunks / 4) windows for a tail of at most SMs / 3
+    assert K.kda_prefill_workspace_size(1, 1024, 1, sm_count=8) == 1 * 19 * slot      # W = 8
+    assert K.kda_prefill_workspace_size(3, 3000, 1, sm_count=8) == 0                 # tail 3 > 8 / 3
+    assert K.kda_prefill_workspace_size(10, 64000, 1, sm_count=8) == 2 * 10 * slot    # 8 + 2 chains, W = 5
+    assert K.kda_prefill_workspace_size(1, 352, 2, sm_count=152) == 0                 # 11 chunks: W would be 2
     assert K.kda_prefill_workspace_size(0, 0, 1, sm_count=152) == 0
     with pytest.raises(K.KdaError):
         K.kda_prefill_workspace_size(1, 100, 0, sm_count=152)
