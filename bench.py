@@ -1,24 +1,27 @@
 #!/usr/bin/env python3
 """KDA hot-path benchmark: chunk-32 prefill + T=1 decode on GB300, one JSON line.
 
-One step = one kda_prefill call over the prefill workload followed by one kda_decode
+One step = one kda_prefill_ex call over the prefill workload followed by one kda_decode
 call over the decode workload (both rows of the hot path), inputs resident in HBM.
-Default workload: prefill 1 x 8192 tokens, H = 8, lower bound -5, FP32 initial state
-N(0, 0.02); decode H = 8, 4096 rows against a 16384-slot FP32 pool, scattered
-unique slots. L2 is flushed (a 512 MiB write) between steps, outside the timed kernel
-segments. ``value`` is prefill tokens*heads/s over the prefill kernel time; decode
-rows*heads/s is reported beside it; ``roofline`` is the kernel with the larger time
-share (the other kernel's roofline sits in its own object).
+Default workload: prefill 8 x 16384 tokens, H = 96, lower bound -8, FP32 initial states
+N(0, 0.02), through kda_prefill_ex with its workspace (five full waves of one CTA per
+chain, the 8 chains left over on the window schedule); decode H = 8, 4096 rows against a
+16384-slot FP32 pool, scattered unique slots. L2 is flushed (a 512 MiB write) between
+steps, outside the timed kernel segments. ``value`` is prefill tokens*heads/s over the
+mean prefill time; decode rows*heads/s is reported beside it; ``roofline`` is the kernel
+with the larger time share (the other kernel's roofline sits in its own object). The
+small-B*H prefill (1 x 8192 tokens, H = 8, windowed) is timed after the main loop and
+reported as ``prefill_small_bh``.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--prefill prefill_h8_t8192|prefill_8x16384_h96|prefill_varlen16_h32|prefill_h1_t64]
+                  [--prefill prefill_8x16384_h96|prefill_h8_t8192|prefill_varlen16_h32|prefill_h1_t64]
                   [--decode-rows R] [--state-dtype f32|bf16] [--no-e2e] [--no-cpu-baseline]
 
 ``--impl reference`` times the FP64 oracle (the CPU reference of this build) on the
 host cores on a bounded sample of the same workload and prints the same JSON shape.
-Under torchrun each rank runs its own copy of the workload (weak scaling: chains are
-independent, so no collective touches the data path); rank 0 prints the line with the
-maximum time over ranks.
+Each rank runs its own copy of the workload (weak scaling: chains are independent, so no
+collective touches the data path); rank 0 prints the line with the maximum time over
+ranks. ``--gpus N`` with N > 1 outside torchrun starts the N rank processes itself.
 """
 from __future__ import annotations
 
@@ -49,7 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--prefill", default="prefill_h8_t8192")
+    p.add_argument("--prefill", default="prefill_8x16384_h96")
     p.add_argument("--decode-rows", type=int, default=4096)
     p.add_argument("--state-dtype", default="f32", choices=["f32", "bf16"])
     p.add_argument("--no-e2e", action="store_true")
@@ -64,6 +67,8 @@ def parse_args(argv=None):
     p.add_argument("--ckpt-every", type=int, default=0,
                    help="prefill also writes the FP32 state every N tokens (a multiple of 32) as checkpoints; "
                         "the e2e and CPU legs are then skipped")
+    p.add_argument("--no-small-bh", action="store_true",
+                   help="skip the secondary 1 x 8192 H8 windowed prefill measurement")
     p.add_argument("--no-windows", action="store_true",
                    help="run kda_prefill (sequential chunk loop) instead of kda_prefill_ex with a workspace")
     return p.parse_args(argv)
@@ -113,22 +118,79 @@ def rank_seed(base: int, rank: int) -> int:
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the timed region runs.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML every 2 ms when libnvidia-ml loads (read-only queries: clock, maximum clock,
+    event reasons), so that even a timed region of a few hundred milliseconds yields many
+    samples; otherwise nvidia-smi every 100 ms. Nothing here changes a GPU setting."""
 
-    def __init__(self, index: int):
-        self.index = index
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, index: int, pci_bus_id: str | None = None, period_s: float = 0.002):
+        self.index, self.pci = index, pci_bus_id
+        self.period = period_s
         self.proc = None
+        self.thread = None
         self.lines = []
+        self.samples = []  # (sm_mhz, reason bits)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+
+    # -- NVML through ctypes (the bindings package is not installed everywhere)
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        rc = 1
+        if self.pci:
+            rc = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(handle))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(handle))
+        if rc != 0:
+            lib.nvmlShutdown()
+            raise OSError("no NVML handle")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        if lib.nvmlDeviceGetMaxClockInfo(handle, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return lib, handle, reasons
+
+    def _nvml_loop(self, lib, handle, reasons):
+        import ctypes
+        mhz, bits = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        try:
+            while not self._stop.is_set():
+                if (lib.nvmlDeviceGetClockInfo(handle, self.NVML_CLOCK_SM, ctypes.byref(mhz)) == 0 and
+                        reasons(handle, ctypes.byref(bits)) == 0):
+                    self.samples.append((float(mhz.value), int(bits.value)))
+                self._stop.wait(self.period)
+        finally:
+            lib.nvmlShutdown()
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+            lib, handle, reasons = self._nvml_open()
+            self.source = "nvml, every 2 ms"
+            self.thread = threading.Thread(target=self._nvml_loop, args=(lib, handle, reasons), daemon=True)
+            self.thread.start()
+            return self
+        except (OSError, AttributeError):
+            pass
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, every 100 ms"
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -140,16 +202,22 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
+        sm, reasons = [], set()
+        smax = [self.max_mhz] if self.max_mhz else []
+        for mhz, bits in self.samples:
+            sm.append(mhz)
+            reasons.update(name for bit, name in self.NVML_REASONS.items() if bits & bit)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
@@ -164,9 +232,19 @@ class ClockSampler:
                 if flag.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax) if smax else None,
+                "sm_min_mhz": min(sm), "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
+
+
+def pci_bus_id(device) -> str | None:
+    """NVML's PCI bus id string of a torch CUDA device, when torch reports its PCI location."""
+    import torch
+    p = torch.cuda.get_device_properties(device)
+    try:
+        return f"{int(p.pci_domain_id):08X}:{int(p.pci_bus_id):02X}:{int(p.pci_device_id):02X}.0"
+    except (AttributeError, TypeError, ValueError):
+        return None
 
 
 # ------------------------------------------------------------------ workloads
@@ -217,6 +295,58 @@ def decode_bytes(rows, heads, state_dtype, tokens=1):
 
 # ------------------------------------------------------------------ our arm
 
+def ms_stats(values):
+    """mean, median and minimum of per-step milliseconds."""
+    return {"mean": sum(values) / len(values), "median": statistics.median(values), "min": min(values)}
+
+
+def prefill_roofline(pcfg, ms, peaks, peak_src, traffic, kernel, extra_bytes=0):
+    """HBM roofline of a prefill schedule over its event time, with the tensor fraction beside it."""
+    p_bytes = prefill_bytes(pcfg) + extra_bytes
+    gbs = p_bytes / (ms * 1e-3) / 1e9
+    flop = prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD
+    tflops = flop / (ms * 1e-3) / 1e12
+    roof = {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 5), "traffic": traffic, "kernel": kernel, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": p_bytes,
+            "tensor": {"achieved": round(tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                       "frac": round(tflops / peaks["bf16_tflops"], 5), "flop_per_launch": flop}}
+    if traffic:
+        roof["frac_of_traffic"] = round(traffic / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)
+    return roof
+
+
+def prefill_schedule(K, pcfg, device, no_windows):
+    """The workspace kda_prefill_ex uses for this workload (None: sequential), the number of
+    chains in full waves ahead of a windowed tail, and the number of launches per call."""
+    import torch
+    ws = None if no_windows else K.prefill_workspace(len(pcfg.seqlens), pcfg.total_tokens, pcfg.num_heads, device)
+    chains = len(pcfg.seqlens) * pcfg.num_heads
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    full_waves = chains // sms if ws is not None else 0
+    # chunk loop (full waves and window 0) + window pass + carry + output pass, or the chunk loop
+    return ws, full_waves, (4 if ws is not None else 1)
+
+
+def schedule_name(ws, full_waves, chains, sms):
+    if ws is None:
+        return "sequential chunk loop"
+    head = (f"{full_waves} full waves of the chunk loop, then {chains - full_waves * sms} chains on "
+            if full_waves else "")
+    return head + f"windows ({ws.numel() >> 20} MiB workspace)"
+
+
+def prefill_traffic(traffic, pcfg, ws, full_waves):
+    """ncu DRAM bytes of one prefill call, scaled from the captured case by units processed: the
+    sequential chunk-loop record for the sequential schedule; for the window schedule the record
+    of the same schedule (all four launches), with or without full waves ahead of it."""
+    units = prefill_units(pcfg)
+    if ws is None:
+        return scaled_traffic(traffic, "kda_prefill_tc_kernel", units)
+    key = "prefill_window_schedule_tail" if full_waves else "prefill_window_schedule_small_bh"
+    return scaled_traffic(traffic, key, units)
+
+
 def run_ours(args):
     import torch
 
@@ -244,13 +374,9 @@ def run_ours(args):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(max(2 * l2, 512 << 20), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    ws = None if args.no_windows else K.prefill_workspace(len(pcfg.seqlens), pcfg.total_tokens, pcfg.num_heads,
-                                                          device)
-    chains = len(pcfg.seqlens) * pcfg.num_heads
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    full_waves = chains // sms if ws is not None else 0  # chains ahead of a windowed tail, one CTA each
-    # chunk loop (full waves and window 0) + window pass + carry + output pass, or the chunk loop
-    prefill_launches = 4 if ws is not None else 1
+    ws, full_waves, prefill_launches = prefill_schedule(K, pcfg, device, args.no_windows)
+    chains = len(pcfg.seqlens) * pcfg.num_heads
 
     ck = ck_off = None
     ck_rows = 0
@@ -288,7 +414,7 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(device)
-    sampler = ClockSampler(local) if not args.no_clocks else None
+    sampler = ClockSampler(local, pci_bus_id(device)) if not args.no_clocks else None
     if sampler:
         sampler.__enter__()
     t_wall = time.perf_counter()
@@ -301,23 +427,29 @@ def run_ours(args):
         ev[s][2].record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t_wall
-    if dist is not None:
-        dist.barrier()
     if sampler:
         sampler.__exit__(None, None, None)
-    p_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
-    d_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
-    p_mean = max_over_ranks(sum(p_ms) / len(p_ms), dist, device)
-    d_mean = max_over_ranks(sum(d_ms) / len(d_ms), dist, device)
+    if dist is not None:
+        dist.barrier()
+    p_st = ms_stats([ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)])
+    d_st = ms_stats([ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)])
+    # the slowest rank sets the time of the job
+    p_st = {k: max_over_ranks(v, dist, device) for k, v in p_st.items()}
+    d_st = {k: max_over_ranks(v, dist, device) for k, v in d_st.items()}
+    p_mean, d_mean = p_st["mean"], d_st["mean"]
     st, detail = K.kda_device_status()
     if st != K.KDA_OK:
         raise RuntimeError(f"device status {st} ({detail}) after the timed region")
+    traffic = load_traffic()
+
+    small = None
+    if not args.no_small_bh and not args.seqlens and not args.heads and args.prefill != "prefill_h8_t8192":
+        small = measure_small_bh(K, args, device, rank, flush, stream, dist, peaks, peak_src, traffic, sms)
 
     e2e = None if args.no_e2e else measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws)
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(pcfg, pin, dcfg, din, pool)
-
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -327,32 +459,28 @@ def run_ours(args):
     d_units = args.decode_rows * dcfg.num_heads * T * world  # (row, head) items x tokens
     p_rate = p_units / (p_mean * 1e-3)
     d_rate = d_units / (d_mean * 1e-3)
-    p_bytes = prefill_bytes(pcfg) + ck_rows * pcfg.num_heads * STATE_BYTES
     d_bytes = decode_bytes(args.decode_rows, dcfg.num_heads, args.state_dtype, T)
-    p_gbs = p_bytes / (p_mean * 1e-3) / 1e9
     d_gbs = d_bytes / (d_mean * 1e-3) / 1e9
-    p_tflops = prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD / (p_mean * 1e-3) / 1e12
-    traffic = load_traffic()
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    waves = math.ceil(len(pcfg.seqlens) * pcfg.num_heads / sms)  # one CTA per chain, one CTA per SM
-    prefill_roof = {"bound": "hbm", "achieved": round(p_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(p_gbs / peaks["hbm_gbs"], 5),
-                    "traffic": (scaled_traffic(traffic, "kda_prefill_tc_kernel", prefill_units(pcfg))
-                                if ws is None and not ck_rows else None),
-                    "kernel": ("kda_prefill_tc_kernel" if ws is None else
-                               ("kda_prefill_tc_kernel full waves + " if full_waves else "") +
-                               "kda_prefill_ex window schedule (window 0, window pass, carry, output pass)"), "peak_source": peak_src,
-                    "algorithmic_bytes_per_launch": p_bytes,
-                    "tensor": {"achieved": round(p_tflops, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                               "frac": round(p_tflops / peaks["bf16_tflops"], 5),
-                               "flop_per_launch": prefill_units(pcfg) * PREFILL_FLOP_PER_TOKEN_HEAD}}
+    waves = math.ceil(chains / sms)  # one CTA per chain, one CTA per SM
+    p_kernel = ("kda_prefill_tc_kernel (sequential chunk loop)" if ws is None else
+                ("kda_prefill_tc_kernel full waves + " if full_waves else "") +
+                "window schedule of the tail (window 0, window pass, carry, output pass)")
+    prefill_roof = prefill_roofline(pcfg, p_mean, peaks, peak_src,
+                                    prefill_traffic(traffic, pcfg, ws, full_waves) if not ck_rows else None, p_kernel,
+                                    extra_bytes=ck_rows * pcfg.num_heads * STATE_BYTES)
     d_kernel = (decode_kernel_name(args.decode_rows * dcfg.num_heads, sms, args.state_dtype) if T == 1
                 else "kda_decode_stream_kernel")
+    d_traffic = (scaled_traffic(traffic, f"{d_kernel}<{args.state_dtype}>", args.decode_rows * dcfg.num_heads)
+                 if T == 1 else None)
     decode_roof = {"bound": "hbm", "achieved": round(d_gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                   "frac": round(d_gbs / peaks["hbm_gbs"], 5),
-                   "traffic": (scaled_traffic(traffic, f"{d_kernel}<{args.state_dtype}>",
-                                              args.decode_rows * dcfg.num_heads) if T == 1 else None),
+                   "frac": round(d_gbs / peaks["hbm_gbs"], 5), "traffic": d_traffic,
                    "kernel": d_kernel, "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes}
+    if d_traffic:
+        decode_roof["frac_of_traffic"] = round(d_traffic / (d_mean * 1e-3) / 1e9 / peaks["hbm_gbs"], 5)
+        if d_traffic < d_bytes:
+            decode_roof["note"] = ("algorithmic bytes exceed the DRAM traffic ncu counts: the last state "
+                                   "writes are still in L2 when the kernel ends, so frac can pass 1.0; "
+                                   "frac_of_traffic is the DRAM-side fraction")
     dominant = prefill_roof if p_mean >= d_mean else decode_roof
     line = {
         "metric": METRIC, "value": round(p_rate, 1), "unit": "tokens*heads/s", "n_gpus": world,
@@ -360,28 +488,32 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool{dcfg.num_slots}",
-                   "prefill": {"seqlens": pcfg.seqlens if len(pcfg.seqlens) <= 16 else f"{len(pcfg.seqlens)} seqs",
+                   "prefill": {"seqlens": pcfg.seqlens if len(set(pcfg.seqlens)) > 1 and len(pcfg.seqlens) <= 16
+                               else f"{len(pcfg.seqlens)} x {pcfg.seqlens[0]}" if len(set(pcfg.seqlens)) == 1
+                               else f"{len(pcfg.seqlens)} seqs",
                                "heads": pcfg.num_heads, "gate": pcfg.gate_mode, "lower_bound": pcfg.lower_bound,
                                "init_state": pcfg.init_std is not None, "ckpt_every": args.ckpt_every},
                    "decode": {"rows": args.decode_rows, "heads": dcfg.num_heads, "pool_slots": dcfg.num_slots,
                               "state_dtype": args.state_dtype, "tokens_per_row": T},
                    "precision": "bf16 operands, tf32 state update, fp32 state and accumulation",
-                   "prefill_schedule": ("sequential chunk loop" if ws is None else
-                                        (f"{full_waves} full waves of the chunk loop, then "
-                                         f"{chains - full_waves * sms} chains on " if full_waves else "") +
-                                        f"windows ({ws.numel() >> 20} MiB workspace)"),
+                   "prefill_schedule": schedule_name(ws, full_waves, chains, sms),
                    "l2": f"flushed between steps ({flush.numel() >> 20} MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "prefill": {"value": round(p_rate, 1), "unit": "tokens*heads/s", "ms": round(p_mean, 4),
+                    "ms_median": round(p_st["median"], 4), "ms_min": round(p_st["min"], 4),
+                    "value_at_median": round(p_units / (p_st["median"] * 1e-3), 1),
                     "us_per_chunk_per_chain": round(p_mean * 1e3 / (math.ceil(max(pcfg.seqlens) / 32) * waves), 4),
                     "waves": waves},
         "decode": {"value": round(d_rate, 1), "unit": "rows*heads/s" if T == 1 else "tokens*heads/s",
-                   "ms": round(d_mean, 4), "roofline": decode_roof},
+                   "ms": round(d_mean, 4), "ms_median": round(d_st["median"], 4), "ms_min": round(d_st["min"], 4),
+                   "roofline": decode_roof},
         "roofline": dominant,
         "roofline_prefill": prefill_roof,
         "gpu_launches": (prefill_launches + 1) * args.steps,
         "wall_s_timed_region": round(wall, 4),
     }
+    if small is not None:
+        line["prefill_small_bh"] = small
     if sampler:
         line["clocks"] = sampler.summary()
     if e2e is not None:
@@ -391,6 +523,44 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+def measure_small_bh(K, args, device, rank, flush, stream, dist, peaks, peak_src, traffic, sms):
+    """The small-B*H prefill (1 x 8192 tokens, H8: 8 chains on the window schedule), timed over
+    --steps calls with L2 flushed between them; reported beside the main line."""
+    import torch
+    cfg, inp = prefill_workload("prefill_h8_t8192", device, rank)
+    ws, full_waves, launches = prefill_schedule(K, cfg, device, args.no_windows)
+    out = torch.empty_like(inp["q"])
+    fin = torch.empty(1, cfg.num_heads, 128, 128, dtype=torch.float32, device=device)
+
+    def call():
+        K.kda_prefill_ex(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"],
+                         inp["init_state"], out, fin, cfg.scale, cfg.lower_bound, cfg.gate_mode, ws, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(device)
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        call()
+        ev[s][1].record(stream)
+    torch.cuda.synchronize(device)
+    st = ms_stats([a.elapsed_time(b) for a, b in ev])
+    st = {k: max_over_ranks(v, dist, device) for k, v in st.items()}
+    units = prefill_units(cfg)
+    world = dist.get_world_size() if dist is not None else 1
+    return {"workload": cfg.name, "value": round(units * world / (st["mean"] * 1e-3), 1), "unit": "tokens*heads/s",
+            "ms": round(st["mean"], 4), "ms_median": round(st["median"], 4), "ms_min": round(st["min"], 4),
+            "us_per_chunk_per_chain": round(st["mean"] * 1e3 / math.ceil(max(cfg.seqlens) / 32), 4),
+            "schedule": schedule_name(ws, full_waves, len(cfg.seqlens) * cfg.num_heads, sms),
+            "gpu_launches": launches * args.steps,
+            "roofline": prefill_roofline(cfg, st["mean"], peaks, peak_src, prefill_traffic(traffic, cfg, ws, full_waves),
+                                         "window schedule (window 0, window pass, carry, output pass)"
+                                         if ws is not None else "kda_prefill_tc_kernel (sequential chunk loop)")}
 
 
 def measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws):
@@ -532,15 +702,17 @@ def oracle_sample(pcfg, pin, dcfg, din, pool, budget_s=20.0):
     import torch
 
     import oracle
-    cpu_p = {k: (v.to("cpu") if v is not None else None) for k, v in pin.items()}
     H = pcfg.num_heads
-    cu = cpu_p["cu_seqlens"].tolist()
+    cu = pin["cu_seqlens"].tolist()
+    # only the first sequence is ever sampled: copy just its tokens to the host
+    cpu_p = {k: pin[k][cu[0]:cu[1]].to("cpu") for k in ("q", "k", "v", "g_raw", "beta")}
+    cpu_p["init_state"] = None if pin["init_state"] is None else pin["init_state"][:1].to("cpu")
     # prefill sample: every head of the first sequence, first `toks` tokens (grown to fill the budget)
     toks = min(512, cu[1] - cu[0])
     res = {}
     while True:
-        sub = {k: (cpu_p[k][:toks] if k in ("q", "k", "v", "g_raw", "beta") else None) for k in cpu_p}
-        init = None if cpu_p["init_state"] is None else cpu_p["init_state"][:1]
+        sub = {k: cpu_p[k][:toks] for k in ("q", "k", "v", "g_raw", "beta")}
+        init = cpu_p["init_state"]
         t0 = time.perf_counter()
         _, _, threads = oracle.prefill(sub["q"], sub["k"], sub["v"], sub["g_raw"], sub["beta"],
                                        torch.tensor([0, toks], dtype=torch.int32), init, scale=pcfg.scale,
@@ -577,9 +749,12 @@ def run_reference(args):
     if world > 1 and rank != 0:
         return None
     import torch
-    pcfg, pin = prefill_workload(args.prefill, "cpu", 0)
-    dcfg = __import__("kda_synth").configs()["decode_h8_pool16384"]
+
     import kda_synth as S
+    # the oracle samples only the first sequence, so only that sequence is drawn on the host
+    first = S.configs()[args.prefill].seqlens[:1]
+    pcfg, pin = prefill_workload(args.prefill, "cpu", 0, seqlens=first)
+    dcfg = S.configs()["decode_h8_pool16384"]
     din = S.decode_inputs(min(args.decode_rows, 1024), dcfg.num_heads, seed=dcfg.seed)
     din["slot_idx"] = torch.arange(din["q"].shape[0], dtype=torch.int32)
     pool = S.state_pool(din["q"].shape[0], dcfg.num_heads, args.state_dtype, std=dcfg.pool_std, seed=dcfg.seed)
@@ -598,8 +773,9 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(wall * 1e3 / max(1, args.steps), 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{pcfg.name} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool{dcfg.num_slots}",
-                       "note": "FP64 CPU oracle on bounded samples of the workload"},
+            "config": {"workload": f"{args.prefill} + decode_h8_rows{args.decode_rows}_{args.state_dtype}_pool{dcfg.num_slots}",
+                       "note": "FP64 CPU oracle on bounded samples of the workload (prefill: a prefix of "
+                               "sequence 0, all heads; decode: the first rows)"},
             "decode": {"value": round(statistics.median(d_rates), 2), "unit": "rows*heads/s"},
             "cpu_baseline": {"value": round(p_rate, 2), "unit": "tokens*heads/s", "cores": r["prefill"][1],
                              "kind": "oracle", "sample": f"prefill: {r['prefill'][2]}; decode: {r['decode'][2]}"},
@@ -607,8 +783,53 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_replicas(n: int, argv, cmd=None, timeout_s=None) -> int:
+    """Starts ranks 0 .. n-1 of this benchmark as child processes on one node (one per GPU), with
+    WORLD_SIZE / RANK / LOCAL_RANK and a 127.0.0.1 rendezvous in their environment, as torchrun
+    would; rank 0 prints the JSON line. If a rank fails, the others are stopped. Returns the
+    first non-zero exit code, else 0."""
+    port = free_port()
+    cmd = cmd or [sys.executable, os.path.abspath(__file__), *argv]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, WORLD_SIZE=str(n), RANK=str(r), LOCAL_RANK=str(r), LOCAL_WORLD_SIZE=str(n),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen(cmd, env=env))
+    t0 = time.monotonic()
+    rc = 0
+    while [p.poll() for p in procs].count(None):  # polls every rank, so each exit code is seen
+        failed = [p.returncode for p in procs if p.returncode not in (None, 0)]
+        late = timeout_s is not None and time.monotonic() - t0 > timeout_s
+        if failed or late:
+            rc = failed[0] if failed else 124
+            for p in procs:
+                if p.poll() is None:
+                    p.terminate()
+            for p in procs:
+                try:
+                    p.wait(timeout=30)
+                except subprocess.TimeoutExpired:
+                    p.kill()
+            break
+        time.sleep(0.05)
+    for p in procs:
+        if rc == 0 and p.returncode:
+            rc = p.returncode
+    return rc
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus, argv))
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -37,6 +37,7 @@ CHUNK = 32
 
 EXPORTED_SYMBOLS = ("kda_prefill", "kda_prefill_ex", "kda_prefill_workspace_size", "kda_prefill_noalloc", "kda_decode",
                     "kda_decode_ex", "kda_status_string", "kda_device_status", "kda_abi_version")
+KDA_NOALLOC_SCRATCH_BYTES = 32 << 20  # fixed scratch array of kda_prefill_noalloc
 KDA_DECODE_L2NORM_QK = 1
 KDA_DECODE_BETA_LOGITS = 2
 KDA_DECODE_MAX_TOKENS = 16
@@ -123,6 +124,12 @@ def _check(t, name, dtype, shape, device):
     del torch
 
 
+def _require_cuda(device):
+    """Host tensors never reach the library: its kernels would read them as device addresses."""
+    if device.type != "cuda":
+        raise ValueError(f"tensors must be on a CUDA device, got {device}")
+
+
 def kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, scale, lower_bound=0.0,
                 gate_mode="lower_bound", stream=None):
     """Varlen chunk-32 prefill into caller-owned ``out`` / ``final_state`` (see include/kda.h)."""
@@ -137,9 +144,11 @@ def kda_prefill(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_state, 
     for name, t in (("init_state", init_state), ("final_state", final_state)):
         if t is not None:
             _check(t, name, torch.float32, (N, H, d, d), dev)
-    st = load().kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
-                            _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
-                            float(lower_bound), _mode(gate_mode), _stream_handle(stream, dev))
+    _require_cuda(dev)
+    with torch.cuda.device(dev):  # the library plans for, and launches on, the current device
+        st = load().kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
+                                _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
+                                float(lower_bound), _mode(gate_mode), _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill")
 
@@ -177,12 +186,14 @@ def kda_prefill_ex(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final_stat
         if workspace.device != dev or not workspace.is_contiguous():
             raise ValueError("workspace: must be a contiguous tensor on the inputs' device")
         nbytes = workspace.numel() * workspace.element_size()
-    st = load().kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
-                               _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
-                               float(lower_bound), _mode(gate_mode), _ptr(checkpoints if ckpt_every else None),
-                               _ptr(ckpt_offsets if ckpt_every else None),
-                               int(checkpoints.shape[0]) if ckpt_every else 0, int(ckpt_every), _ptr(workspace),
-                               nbytes, _stream_handle(stream, dev))
+    _require_cuda(dev)
+    with torch.cuda.device(dev):  # the window plan follows the current device's SM count
+        st = load().kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
+                                   _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
+                                   float(lower_bound), _mode(gate_mode), _ptr(checkpoints if ckpt_every else None),
+                                   _ptr(ckpt_offsets if ckpt_every else None),
+                                   int(checkpoints.shape[0]) if ckpt_every else 0, int(ckpt_every),
+                                   _ptr(workspace), nbytes, _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_ex")
 
@@ -203,9 +214,11 @@ def kda_prefill_noalloc(q, k, v, g_raw, beta, cu_seqlens, init_state, out, final
     for name, t in (("init_state", init_state), ("final_state", final_state)):
         if t is not None:
             _check(t, name, torch.float32, (N, H, d, d), dev)
-    st = load().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
-                                    _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
-                                    float(lower_bound), _mode(gate_mode), _stream_handle(stream, dev))
+    _require_cuda(dev)
+    with torch.cuda.device(dev):  # the scratch array and the plan are those of the current device
+        st = load().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(cu_seqlens),
+                                        _ptr(init_state), _ptr(out), _ptr(final_state), N, T, H, float(scale),
+                                        float(lower_bound), _mode(gate_mode), _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_noalloc")
 
@@ -262,10 +275,12 @@ def _decode_call(name, q, k, v, g_raw, beta, slot_idx, state_pool, out, scale, l
     head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta), _ptr(slot_idx), _ptr(state_pool),
             int(state_pool.shape[0]), sdt, _ptr(out), R)
     tail = (float(scale), float(lower_bound), _mode(gate_mode))
-    if name == "kda_decode":
-        st = lib.kda_decode(*head, H, *tail, _stream_handle(stream, dev))
-    else:
-        st = lib.kda_decode_ex(*head, T, H, *tail, int(flags), float(norm_eps), _stream_handle(stream, dev))
+    _require_cuda(dev)
+    with torch.cuda.device(dev):  # the schedule follows the current device's SM count
+        if name == "kda_decode":
+            st = lib.kda_decode(*head, H, *tail, _stream_handle(stream, dev))
+        else:
+            st = lib.kda_decode_ex(*head, T, H, *tail, int(flags), float(norm_eps), _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, name)
 

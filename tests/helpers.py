@@ -77,3 +77,15 @@ def oracle_prefill(inp: dict, *, scale, lower_bound, gate_mode, threads=0):
                                  inp.get("init_state"), scale=scale, lower_bound=lower_bound, gate_mode=gate_mode,
                                  threads=threads)
     return out, fin
+
+
+def launch_order(seqlens, num_heads, ranked_max=256):
+    """(sequence, head) of each launch position of the prefill: head p % H of the sequence
+    ranked p // H by length, longest first, ties by index (batches of more than
+    ``ranked_max`` sequences keep index order). The windowed tail of kda_prefill_ex is the
+    last ``chains % SMs`` positions."""
+    N = len(seqlens)
+    ranked = list(range(N))
+    if 1 < N <= ranked_max:
+        ranked.sort(key=lambda n: (-seqlens[n], n))
+    return [(ranked[p // num_heads], p % num_heads) for p in range(N * num_heads)]

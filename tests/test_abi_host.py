@@ -153,6 +153,8 @@ def test_binding_checks_dtypes_and_shapes_before_calling(lib):
         K.kda_prefill(q, q, q, q, beta[:3], cu, None, q, None, 0.1)
     with pytest.raises(TypeError):
         K.kda_decode(q, q, q, q, beta, torch.zeros(4, dtype=torch.int64), torch.zeros(8, 2, 128, 128), q, 0.1)
+    with pytest.raises(ValueError, match="CUDA device"):  # host tensors never reach the library
+        K.kda_prefill(q, q, q, q, beta, cu, None, q, None, 0.1)
 
 
 def test_product_path_has_no_fallback(monkeypatch, tmp_path):
@@ -184,3 +186,19 @@ def test_window_plan_on_host(lib):
         K.kda_prefill_workspace_size(1, 100, 0, sm_count=152)
     with pytest.raises(K.KdaError):
         K.kda_prefill_workspace_size(1, 100, 1, sm_count=-1)
+
+
+def test_noalloc_scratch_bound_on_host(lib):
+    """Every window plan needs at most 3 SMs - 2 FP32 states, so the fixed 32 MiB array of
+    kda_prefill_noalloc holds every plan on GPUs of up to 171 SMs (host arithmetic only)."""
+    slot = 128 * 128 * 4
+    for sms in (8, 76, 148, 152, 160, 171):
+        worst = 0
+        for tail in range(1, sms // 3 + 1):
+            # `tail` chains left over past full waves, each long enough for sms / tail + 1 windows
+            seqs = sms + tail
+            toks = seqs * (sms // tail + 1) * 4 * 32
+            worst = max(worst, K.kda_prefill_workspace_size(seqs, toks, 1, sm_count=sms))
+        assert worst == (3 * sms - 2) * slot, sms  # reached by a tail of one chain
+        assert worst <= K.KDA_NOALLOC_SCRATCH_BYTES
+    assert (3 * 172 - 2) * slot > K.KDA_NOALLOC_SCRATCH_BYTES

@@ -56,3 +56,50 @@ def test_rank_seed_is_distinct_and_stable():
     import bench
     seeds = {bench.rank_seed(1, r) for r in range(8)}
     assert len(seeds) == 8 and bench.rank_seed(1, 0) == 1
+
+
+CHILD = r'''
+import json, os, sys
+sys.path.insert(0, {root!r})
+import bench
+world, rank, local = bench.dist_env()
+if os.environ.get("FAIL_RANK") == str(rank):
+    sys.exit(3)
+d = bench.init_dist(world, "gloo")
+t = bench.max_over_ranks(10.0 + rank, d)
+d.barrier()
+if rank == 0:
+    print(json.dumps({{"world": world, "max": t, "local": local, "addr": os.environ["MASTER_ADDR"]}}), flush=True)
+d.destroy_process_group()
+'''
+
+
+@pytest.mark.timeout(180)
+def test_gpus_flag_launches_replicas_itself(tmp_path, capfd):
+    """bench.py --gpus N outside torchrun starts N rank processes with the torchrun environment;
+    rank 0 alone prints, with the maximum over ranks."""
+    import json
+
+    import bench
+    script = tmp_path / "child.py"
+    script.write_text(CHILD.format(root=bench.ROOT))
+    import sys
+    rc = bench.launch_replicas(2, [], cmd=[sys.executable, str(script)], timeout_s=150)
+    out = capfd.readouterr().out.strip().splitlines()
+    assert rc == 0
+    lines = [json.loads(x) for x in out if x.startswith("{")]
+    assert lines == [{"world": 2, "max": 11.0, "local": 0, "addr": "127.0.0.1"}]
+
+
+@pytest.mark.timeout(180)
+def test_replica_launcher_stops_the_job_when_a_rank_fails(tmp_path, monkeypatch):
+    """A rank that exits with an error ends the job with its code; the rank left waiting in the
+    rendezvous is stopped instead of hanging."""
+    import sys
+
+    import bench
+    script = tmp_path / "child.py"
+    script.write_text(CHILD.format(root=bench.ROOT))
+    monkeypatch.setenv("FAIL_RANK", "1")
+    rc = bench.launch_replicas(2, [], cmd=[sys.executable, str(script)], timeout_s=150)
+    assert rc == 3

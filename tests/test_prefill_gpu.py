@@ -9,7 +9,7 @@ import torch
 
 import kda_recurrent_gb300 as K
 import kda_synth as S
-from helpers import (assert_out_close, assert_state_close, oracle_prefill, slice_problem)
+from helpers import (assert_out_close, assert_state_close, launch_order, oracle_prefill, slice_problem)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -66,7 +66,9 @@ def test_cfg_h8_t8192():
 
 
 def test_cfg_varlen16_h32_sampled_heads():
-    """Full launch (all 32 heads); the oracle checks 6 heads over all 16 sequences."""
+    """Full launch (all 32 heads); the oracle checks 6 heads over all 16 sequences and all 32
+    heads of four sequences: the longest (3747 tokens, ragged), the shortest (307), one whose
+    last chunk holds a single token (449) and one that ends on a chunk boundary (2112)."""
     cfg = S.configs()["prefill_varlen16_h32"]
     inp = S.config_inputs(cfg)
     out, fin = gpu_prefill(inp, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
@@ -75,12 +77,29 @@ def test_cfg_varlen16_h32_sampled_heads():
     ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
     assert_out_close(out[:, heads], ref_out)
     assert_state_close(fin[:, heads], ref_fin)
+    lens = cfg.seqlens
+    seqs = [lens.index(max(lens)), lens.index(min(lens)), lens.index(449), lens.index(2112)]
+    assert lens[seqs[0]] % 32 and lens[seqs[2]] % 32 == 1 and lens[seqs[3]] % 32 == 0
+    sub = slice_problem(inp, seqs=seqs)
+    ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
+    assert_out_close(out[sub["token_index"]], ref_out)
+    assert_state_close(fin[seqs], ref_fin)
 
 
-def test_cfg_8x16384_h96_sampled_chains():
-    """Full-size launch as the bench times it; the oracle checks 2 heads of every sequence."""
+@pytest.fixture(scope="module")
+def cfg5():
+    """The 8 x 16384 H96 lb = -8 workload on the device, drawn as the bench draws it."""
     cfg = S.configs()["prefill_8x16384_h96"]
     inp = S.config_inputs(cfg, device=DEV)
+    yield cfg, inp
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_cfg_8x16384_h96_sampled_chains(cfg5):
+    """Full-size launch on the sequential schedule (kda_prefill); the oracle checks 2 heads of
+    every sequence."""
+    cfg, inp = cfg5
     out, fin = K.prefill(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"],
                          inp["init_state"], scale=SCALE, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
     assert K.kda_device_status()[0] == K.KDA_OK
@@ -89,6 +108,40 @@ def test_cfg_8x16384_h96_sampled_chains():
     ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
     assert_out_close(out[:, heads].cpu(), ref_out)
     assert_state_close(fin[:, heads].cpu(), ref_fin)
+
+
+def test_cfg_8x16384_h96_as_benched(cfg5):
+    """The schedule the bench times: kda_prefill_ex with its workspace, i.e. full waves of one
+    CTA per chain and the chains of the short last wave cut into windows (window 0, window
+    pass, carry, output pass) at lb = -8. The oracle checks every windowed chain and 2 heads of
+    every sequence from the full waves."""
+    cfg, inp = cfg5
+    N, H, T = len(cfg.seqlens), cfg.num_heads, cfg.total_tokens
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    ws = K.prefill_workspace(N, T, H, DEV)
+    tail = (N * H) % sms
+    assert ws is not None and 0 < 3 * tail <= sms, "this workload has a windowed tail on this GPU"
+    out, fin = K.prefill(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"],
+                         inp["init_state"], scale=SCALE, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode,
+                         workspace=ws)
+    st, detail = K.kda_device_status()
+    assert st == K.KDA_OK, (st, detail)
+    order = launch_order(cfg.seqlens, H)
+    windowed = order[N * H - tail:]
+    assert len({n for n, _ in windowed}) == 1  # equal lengths: the last heads of the last sequence
+    n_t = windowed[0][0]
+    t_heads = [h for _, h in windowed]
+    sub = slice_problem(inp, heads=t_heads, seqs=[n_t])
+    ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
+    cu = inp["cu_seqlens"].tolist()
+    assert_out_close(out[cu[n_t]:cu[n_t + 1], t_heads].cpu(), ref_out, what="windowed out")
+    assert_state_close(fin[n_t, t_heads].cpu()[None], ref_fin, what="windowed state")
+    full = [5, 61]
+    assert not set(full) & set(t_heads)
+    sub = slice_problem(inp, heads=full)
+    ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=cfg.lower_bound, gate_mode=cfg.gate_mode)
+    assert_out_close(out[:, full].cpu(), ref_out)
+    assert_state_close(fin[:, full].cpu(), ref_fin)
 
 
 def test_split_at_chunk_boundaries_is_bitwise():

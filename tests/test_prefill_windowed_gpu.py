@@ -66,6 +66,17 @@ def test_windowed_slow_decay_carries_the_state(rate):
     check(inp, lower_bound=0.0, gate_mode="log_decay")
 
 
+@pytest.mark.parametrize("lens", [[3000], [1500, 3000, 610]], ids=["1x3000", "varlen3"])
+def test_windowed_lower_bound_minus_8(lens):
+    """lb = -8, the widest exponent range of the half-chunk anchors, on the window schedule with
+    an initial state: the window maps M are built through the same anchored operands."""
+    inp = S.prefill_inputs(lens, 2, seed=38 + len(lens), init_std=0.02)
+    N, T = len(lens), sum(lens)
+    slots = K.kda_prefill_workspace_size(N, T, 2, sm_count=152) // (N * 2 * 128 * 128 * 4)
+    assert (slots + 5) // 3 >= 4, "a plan of at least 4 windows per chain (3 W - 5 state slots)"
+    check(inp, lower_bound=-8.0, gate_mode="lower_bound")
+
+
 def test_windowed_ragged_multi_sequence():
     inp = S.prefill_inputs([1000, 37, 0, 2500, 130], 2, seed=32, init_std=0.02)
     check(inp, lower_bound=0.0, gate_mode="softplus")
