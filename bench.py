@@ -344,7 +344,7 @@ def prefill_traffic(traffic, pcfg, ws, full_waves):
     if ws is None:
         return scaled_traffic(traffic, "kda_prefill_tc_kernel", units)
     key = "prefill_window_schedule_tail" if full_waves else "prefill_window_schedule_small_bh"
-    return scaled_traffic(traffic, key, units)
+    return scaled_traffic(traffic, key, units, len(pcfg.seqlens) * pcfg.num_heads)
 
 
 def run_ours(args):
@@ -687,12 +687,13 @@ def load_traffic():
     return out
 
 
-def scaled_traffic(traffic, kernel, units):
-    """ncu DRAM bytes per launch, scaled from the captured case to this launch by units processed."""
+def scaled_traffic(traffic, kernel, units, chains=0):
+    """ncu DRAM bytes per launch, scaled from the captured case to this launch by units processed
+    (plus, where the record separates it, the state traffic of each chain)."""
     rec = traffic.get(kernel)
     if rec is None:
         return None
-    return int(rec["dram_bytes_per_unit"] * units)
+    return int(rec["dram_bytes_per_unit"] * units + rec.get("dram_bytes_per_chain", 0) * chains)
 
 
 # ------------------------------------------------------------------ oracle timing (CPU baseline)

@@ -66,30 +66,35 @@ def load(build_if_missing: bool = False):
                 if not build_if_missing:
                     raise RuntimeError(f"KDA CUDA library not built: {path} (run kda_recurrent_gb300.build.build())")
                 _build.build()
-            lib = ctypes.CDLL(path)
-            vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
-            lib.kda_prefill.restype = ctypes.c_int
-            lib.kda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
-            lib.kda_prefill_ex.restype = ctypes.c_int
-            lib.kda_prefill_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp, vp,
-                                           i64, i32, vp, i64, vp]
-            lib.kda_prefill_workspace_size.restype = ctypes.c_int64
-            lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
-            lib.kda_prefill_noalloc.restype = ctypes.c_int
-            lib.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
-            lib.kda_decode.restype = ctypes.c_int
-            lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, vp]
-            lib.kda_decode_ex.restype = ctypes.c_int
-            lib.kda_decode_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, f32, f32, i32, i32,
-                                          f32, vp]
-            lib.kda_status_string.restype = ctypes.c_char_p
-            lib.kda_status_string.argtypes = [ctypes.c_int]
-            lib.kda_device_status.restype = ctypes.c_int
-            lib.kda_device_status.argtypes = [vp, ctypes.POINTER(i32)]
-            lib.kda_abi_version.restype = ctypes.c_int
-            lib.kda_abi_version.argtypes = []
-            _lib = lib
+            _lib = bind(ctypes.CDLL(path))
     return _lib
+
+
+def bind(lib):
+    """Declares the argument and result types of every C entry point on a loaded library
+    handle (the product library, or a test build of the same sources)."""
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
+    lib.kda_prefill_ex.restype = ctypes.c_int
+    lib.kda_prefill_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp, vp,
+                                   i64, i32, vp, i64, vp]
+    lib.kda_prefill_workspace_size.restype = ctypes.c_int64
+    lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.kda_prefill_noalloc.restype = ctypes.c_int
+    lib.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, vp]
+    lib.kda_decode.restype = ctypes.c_int
+    lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, f32, f32, i32, vp]
+    lib.kda_decode_ex.restype = ctypes.c_int
+    lib.kda_decode_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, f32, f32, i32, i32,
+                                  f32, vp]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_device_status.restype = ctypes.c_int
+    lib.kda_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.kda_abi_version.restype = ctypes.c_int
+    lib.kda_abi_version.argtypes = []
+    return lib
 
 
 def kda_status_string(status: int) -> str:

@@ -332,9 +332,13 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
             slot_next = slot_of(item + 2 * stride);
             if (gt < TT) beta_next = a.beta[tok_index(item + 2 * stride, gt)];
         }
-        if (!mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u)) {
-            report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
-            break;
+        {  // one decision for the whole group, so that a wait that gave up in some threads only
+           // cannot split the group at its next barrier
+            const bool got = mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u);
+            if (bar_any(2 + grp, 128, !got)) {
+                if (!got) report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+                break;
+            }
         }
         if (slot < 0) {
             for (int t = 0; t < TT; ++t) a.out[tok_index(item, t) * kHeadDim + gt] = __float2bfloat16_rn(0.0f);
@@ -502,6 +506,11 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
         auto issue = [&](int kk) {
             const int st = kk % NS;
             const int64_t item = first + (int64_t)kk * stride;
+#ifdef KDA_TEST_WITHHOLD_HANDOFF
+            // failure-detection test build only: the fill of this item is lost, so the compute
+            // warps' bounded wait for it runs out and the CTA takes its abort path
+            if (kk == KDA_TEST_WITHHOLD_HANDOFF) return;
+#endif
             const int64_t slot = slot_of(item);
             if (slot < 0) {
                 mbar_arrive(&full[st]);
@@ -522,11 +531,15 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                     bulk_load(smem_addr(tdst + m * kHeadDim * 2), rows[m], kHeadDim * 2, &full[st]);
             }
         };
-        for (int kk = 0; kk < NS && kk < mine; ++kk) issue(kk);
+        int issued = 0;
+        for (int kk = 0; kk < NS && kk < mine; ++kk) issue(kk), issued = kk + 1;
         for (int j = 0; j < mine; ++j) {
             const int st = j % NS;
             if (!mbar_wait(&done[st], (uint32_t)(j / NS) & 1u)) {
                 report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+                // the fills of items j .. issued - 1 may still be writing their stages (one per
+                // stage): wait for them, bounded, before the CTA's shared memory is released
+                for (int kk = j; kk < issued; ++kk) mbar_wait(&full[kk % NS], (uint32_t)(kk / NS) & 1u);
                 break;
             }
             const int64_t item = first + (int64_t)j * stride;
@@ -543,6 +556,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             if (j >= 1 && j - 1 + NS < mine) {
                 bulk_wait_read_but_newest();
                 issue(j - 1 + NS);
+                issued = j + NS;
             }
         }
         bulk_wait_all();
@@ -567,10 +581,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             slot_next = slot_of(item + stride);
             if (tid < TT) beta_next = a.beta[tok_index(item + stride, tid)];
         }
-        if (!mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u)) {
-            report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
-            break;
-        }
+        const bool got = mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u);
         if (slot < 0) {
             if (tid < kHeadDim)
                 for (int t = 0; t < TT; ++t) a.out[tok_index(item, t) * kHeadDim + tid] = __float2bfloat16_rn(0.0f);
@@ -593,7 +604,13 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
         // (c mod RPP) NPASS + c / RPP, so that the NPASS rows a thread owns are contiguous.
         const __nv_bfloat16 *const rows0 =
             reinterpret_cast<const __nv_bfloat16 *>(stages + (size_t)st * stage_bytes + SS::kItemBytes);
-        compute_bar();  // the previous item's use of the shared vectors is over
+        // the previous item's use of the shared vectors is over; and one decision for all
+        // compute threads on the wait above (a wait that gave up in some threads only must not
+        // split them at the barriers that follow)
+        if (bar_any(1, kDecodeThreads, !got)) {
+            if (!got) report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+            break;
+        }
         for (int x = tid; x < TT * kHeadDim; x += kDecodeThreads) {
             const int t = x >> 7, c = x & (kHeadDim - 1);
             const int pc = (c % RPP) * NPASS + c / RPP;

@@ -127,6 +127,7 @@ struct Bars {
     uint64_t ab_empty;   // group B -> A: the pair operands of a chunk consumed
                          //   (count kSolveThreads, one phase per chunk)
     uint64_t vfree;      // group B -> A: the raw v, beta of a chunk consumed (same counting)
+    uint64_t drain;      // after an abort: the two MMA-issuing threads' work complete (count 2)
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -140,21 +141,6 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ void bar_named(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Named-barrier sync of `count` threads that also returns, identically to all of them,
-// whether `pred` held for any of them.
-__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
 }
 
 // Bounded wait; on expiry records a timeout and raises the CTA's abort flag.
@@ -749,6 +735,11 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         kt_to_stage(tmem, stage, bwarp, lane);
         fence_async_smem();
         tc_fence_before();
+#ifdef KDA_TEST_WITHHOLD_HANDOFF
+        // failure-detection test build only: the hand-off of this chunk is lost, so the state
+        // warps' bounded wait for it runs out and the CTA takes its abort path
+        if (c == KDA_TEST_WITHHOLD_HANDOFF) continue;
+#endif
         mbar_arrive(&B->prep[ps]);
     }
 }
@@ -1171,6 +1162,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         mbar_init(&B->g2s[1], 1);
         mbar_init(&B->oread[0], kStateThreads);
         mbar_init(&B->oread[1], kStateThreads);
+        mbar_init(&B->drain, 2);
         B->abort = 0;
         fence_mbar_init();
     }
@@ -1202,14 +1194,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
             const int chunk_base = sp.lw * w;
             state_loop(a, smem, B, tmem, n, h, bos, eos, nchunks, chunk_base, init, fin);
         }
-        if (B->abort != 0 && warp == kFirstStateWarp && (threadIdx.x & 31) == 0) {
-            // drain any MMA still in flight before the tensor memory is released
-            mma_commit(&B->g1);
-            mbar_wait(&B->g1, 0);
-            mbar_wait(&B->g1, 1);
-        }
     }
     tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // After an abort (every group has left its loop, so all threads read the same flag), the
+    // two threads that issue MMAs drain whatever they still have in flight before the tensor
+    // memory is released; the wait is bounded like every other.
+    if (B->abort != 0 && (threadIdx.x == kKtThread || threadIdx.x == kFirstStateWarp * 32)) {
+        mma_commit(&B->drain);
+        mbar_wait(&B->drain, 0);
+        tc_fence_before();
+    }
     __syncthreads();
     tc_fence_after();
     if (warp == kFirstStateWarp) tmem_dealloc(tmem, kTmemCols);

@@ -13,7 +13,12 @@
 
 namespace kda {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait that lasts 2 s is treated as lost
+// A wait that lasts 2 s is treated as lost. The failure-detection test builds a separate
+// copy of the library with a 1 ms limit (and one hand-off withheld) to exercise that path.
+#ifndef KDA_WAIT_LIMIT_NS
+#define KDA_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = KDA_WAIT_LIMIT_NS;
 constexpr uint32_t kSuspendHintNs = 1000000u;      // hardware suspend hint per try_wait
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -61,6 +66,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
             return false;
         }
     }
+}
+
+// Named-barrier sync of `count` threads that also returns, identically to all of them,
+// whether `pred` held for any of them. Used after a bounded wait, so that a wait that gave
+// up in some threads only never splits a group at its next barrier.
+__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- TMEM allocation
