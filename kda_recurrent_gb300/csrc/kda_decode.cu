@@ -243,6 +243,7 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_but_newest() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
@@ -335,7 +336,7 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
         {  // one decision for the whole group, so that a wait that gave up in some threads only
            // cannot split the group at its next barrier
             const bool got = mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u);
-            if (bar_any(2 + grp, 128, !got)) {
+            if (grp == 0 ? bar_any(2, 128, !got) : bar_any(3, 128, !got)) {
                 if (!got) report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
                 break;
             }
@@ -447,10 +448,12 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
 // updated state is back in the stage; the producer then stores it with a bulk copy. It
 // refills a stage with the state NS items ahead one item later, once the store has read
 // the stage: waiting for that read right after issuing the store kept the producer from
-// issuing anything else for the length of the read. With
-// several tokens per row the state stays in registers while its tokens are applied in
-// order, and is stored once.
-template <typename T>
+// issuing anything else for the length of the read. A ring of only two stages (FP32 states
+// with 6 or more tokens per row) is the exception (kRefillAtOnce): there the deferred refill
+// would start the next item's load only once the compute warps want it, so each stage is
+// refilled as soon as its store has read it. With several tokens per row the state stays in
+// registers while its tokens are applied in order, and is stored once.
+template <typename T, bool kRefillAtOnce>
 __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kernel(DecodeArgs a) {
     using V = StateVec<T>;
     using SS = StreamShape<T>;
@@ -551,9 +554,16 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                     bulk_store(dst + p, smem_addr(stages + (size_t)st * stage_bytes + p), SS::kPiece);
             }
             bulk_commit();  // one group per item, empty for a skipped one
-            // the stage of the previous item is refilled once its store has read it, which
-            // has had this item's wait to happen in
-            if (j >= 1 && j - 1 + NS < mine) {
+            if constexpr (kRefillAtOnce) {
+                // this item's stage takes the item NS ahead as soon as the store has read it
+                if (j + NS < mine) {
+                    bulk_wait_read_all();
+                    issue(j + NS);
+                    issued = j + NS + 1;
+                }
+            } else if (j >= 1 && j - 1 + NS < mine) {
+                // the stage of the previous item is refilled once its store has read it, which
+                // has had this item's wait to happen in
                 bulk_wait_read_but_newest();
                 issue(j - 1 + NS);
                 issued = j + NS;
@@ -710,22 +720,31 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     }
 }
 
-template <typename T>
-cudaError_t launch_decode_stream(const DecodeArgs &a, cudaStream_t stream, int sms) {
+template <typename T, bool kRefillAtOnce>
+cudaError_t launch_decode_stream_t(const DecodeArgs &a, cudaStream_t stream, int sms) {
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kda_decode_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 StreamShape<T>::kStreamSmem);
+        e = cudaFuncSetAttribute(kda_decode_stream_kernel<T, kRefillAtOnce>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, StreamShape<T>::kStreamSmem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     const int64_t items = (int64_t)a.rows * a.num_heads;
     const int grid = (int)std::min<int64_t>(items, sms);
-    kda_decode_stream_kernel<T><<<grid, kDecodeThreads + 32, StreamShape<T>::smem(a.tokens), stream>>>(a);
+    kda_decode_stream_kernel<T, kRefillAtOnce>
+        <<<grid, kDecodeThreads + 32, StreamShape<T>::smem(a.tokens), stream>>>(a);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_decode_stream(const DecodeArgs &a, cudaStream_t stream, int sms) {
+    // BF16 rings keep an even stage count of at least four
+    if constexpr (!StreamShape<T>::kGroups)
+        if (StreamShape<T>::stages(a.tokens) <= 2) return launch_decode_stream_t<T, true>(a, stream, sms);
+    return launch_decode_stream_t<T, false>(a, stream, sms);
 }
 
 template <typename T, int JW>
