@@ -190,7 +190,10 @@ KDA_API int kda_prefill_noalloc(const void *q, const void *k, const void *v, con
  *   v            BF16 [rows, num_heads, 128]
  *   beta         FP32 [rows, num_heads]
  *   slot_idx     int32 [rows], device. Row r updates pool slot slot_idx[r] for every
- *                head. Slots must be unique (duplicates race; not detected). A
+ *                head. Slots must be unique: rows that share a slot race on it. A build
+ *                compiled with KDA_DEBUG_CHECKS first compares every row with the earlier
+ *                ones and records the later row of a repeated slot as KDA_ERR_DEVICE_INPUT
+ *                (quadratic in rows; the product build does not check). A
  *                negative slot marks a padding row: its outputs are written as
  *                zeros and no state is touched. A slot >= num_slots is treated as
  *                padding and recorded as KDA_ERR_DEVICE_INPUT.

@@ -130,11 +130,15 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
     constexpr int RPP = kDecodeThreads / VPR; // rows covered by one pass of the CTA
     constexpr int NPASS = kHeadDim / RPP;     // passes (vectors held per thread)
     constexpr int NSPLIT = kHeadDim / JW;     // column blocks per item
+    // column sums: G threads per (vector, column), each adding PER rows of the partial sums
+    constexpr int G = kDecodeThreads / (2 * JW);
+    constexpr int PER = RPP / G;
     static_assert(kDecodeThreads % VPR == 0 && kHeadDim % RPP == 0, "tile shape");
-    static_assert(2 * JW <= kDecodeThreads, "one reducer thread per column sum");
+    static_assert(2 * JW <= kDecodeThreads && kDecodeThreads % (2 * JW) == 0 && RPP % G == 0, "column sums");
 
     __shared__ float s_k[kHeadDim], s_q[kHeadDim], s_decay[kHeadDim];
     __shared__ float s_red[2][RPP][JW];
+    __shared__ float s_part[2][G][JW];
     __shared__ float s_u[JW];
 
     const int tid = threadIdx.x;
@@ -167,8 +171,14 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
         raw[p] = __ldcs(reinterpret_cast<const typename V::Raw *>(S + off));
     }
 
-    // 2. Token vectors and the per-channel decay while the state is in flight.
+    // 2. Token vectors and the per-channel decay while the state is in flight; the column
+    //    threads also fetch v and beta now, off the path that follows the column sums.
     const size_t tok = (size_t)item * kHeadDim;
+    float v_col = 0.0f, beta_item = 0.0f;
+    if (tid < JW) {
+        v_col = __bfloat162float(a.v[tok + j0 + tid]);
+        beta_item = beta_of(a.beta[item], a);
+    }
     if (tid < kHeadDim) {
         const float av = __bfloat162float(a.g_raw[tok + tid]);
         s_decay[tid] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
@@ -202,15 +212,26 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(DecodeArgs a
     }
     __syncthreads();
 
-    // 4. Column sums, the delta-rule residual u and the output, one thread per column.
+    // 4. Column sums in two levels over all threads (a warp reads one row of 32 columns per
+    //    step, so without bank conflicts), then the delta-rule residual u and the output, one
+    //    thread per column.
+    {
+        const int col = tid % JW, rest = tid / JW;
+        const int vec = rest & 1, part = rest >> 1;
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc += s_red[vec][part * PER + i][col];
+        s_part[vec][part][col] = acc;
+    }
+    __syncthreads();
     if (tid < JW) {
         float w_k = 0.0f, w_q = 0.0f;
-#pragma unroll 8
-        for (int i = 0; i < RPP; ++i) {
-            w_k += s_red[0][i][tid];
-            w_q += s_red[1][i][tid];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            w_k += s_part[0][g][tid];
+            w_q += s_part[1][g][tid];
         }
-        const float u = beta_of(a.beta[item], a) * (__bfloat162float(a.v[tok + j0 + tid]) - w_k);
+        const float u = beta_item * (v_col - w_k);
         s_u[tid] = u;
         out[tid] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
     }
@@ -353,7 +374,9 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
         for (int t = 0; t < TT; ++t) {
             const __nv_bfloat16 *trow =
                 reinterpret_cast<const __nv_bfloat16 *>(S + SS::kItemBytes + t * SS::kTokBytes);
-            gbar();  // the previous step's use of the group's vectors (and state slice) is over
+            // the previous step's use of the group's vectors (and state slice) is over; before
+            // the first token the group barrier after the stage wait has already made sure
+            if (t > 0) gbar();
             {
                 const float av = __bfloat162float(trow[2 * kHeadDim + gt]);
                 s_decay[gt] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
@@ -760,7 +783,8 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
 int pick_decode_width(int64_t items) {
     if (items >= 1024) return 128;
     if (items >= 256) return 64;
-    return 32;
+    if (items >= 64) return 32;
+    return 16;
 }
 
 // Items per SM from which the streaming schedule takes over (several per SM, so that its
@@ -771,8 +795,30 @@ constexpr int kStreamItemsPerSmBF16 = 3;
 
 }  // namespace
 
+#ifdef KDA_DEBUG_CHECKS
+// Debug builds only: a slot named by two rows is recorded as KDA_ERR_DEVICE_INPUT with the
+// later row as its detail (the decode of such a batch races on that slot). Padding rows
+// (negative slots) may repeat. Every row is compared with every earlier one: quadratic, for
+// debugging only.
+__global__ void kda_check_slots_kernel(const int32_t *slot_idx, int32_t rows, DeviceStatus *status) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    const int32_t s = __ldg(slot_idx + r);
+    if (s < 0) return;
+    for (int q = 0; q < r; ++q)
+        if (__ldg(slot_idx + q) == s) {
+            report_error(status, KDA_ERR_DEVICE_INPUT, r);
+            return;
+        }
+}
+#endif
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     const int64_t items = (int64_t)a.rows * a.num_heads;
+#ifdef KDA_DEBUG_CHECKS
+    kda_check_slots_kernel<<<(a.rows + 255) / 256, 256, 0, stream>>>(a.slot_idx, a.rows, a.status);
+    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
+#endif
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -786,11 +832,13 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     if (a.state_dtype == KDA_STATE_F32) {
         if (jw == 128) return launch_decode_t<float, 128>(a, stream);
         if (jw == 64) return launch_decode_t<float, 64>(a, stream);
-        return launch_decode_t<float, 32>(a, stream);
+        if (jw == 32) return launch_decode_t<float, 32>(a, stream);
+        return launch_decode_t<float, 16>(a, stream);
     }
     if (jw == 128) return launch_decode_t<__nv_bfloat16, 128>(a, stream);
     if (jw == 64) return launch_decode_t<__nv_bfloat16, 64>(a, stream);
-    return launch_decode_t<__nv_bfloat16, 32>(a, stream);
+    if (jw == 32) return launch_decode_t<__nv_bfloat16, 32>(a, stream);
+    return launch_decode_t<__nv_bfloat16, 16>(a, stream);
 }
 
 }  // namespace kda
