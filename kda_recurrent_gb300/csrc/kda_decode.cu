@@ -290,7 +290,7 @@ struct StreamShape {
     // FP32 states: the partial sums, u and beta, then the decay, k and q vectors of every
     // token of the item ([tokens][3][128], filled once per item); the mbarriers last
     static constexpr int kScalars = kRed + kHeadDim * 4 + kMaxTokensPerRow * 4 + kMaxTokensPerRow * 16;
-    static constexpr int kBarBytes = 2 * kMaxStages * 8;
+    static constexpr int kBarBytes = 2 * kMaxStages * 8 + 16;  // full[], done[], two abort flags
     static __host__ __device__ int fixed(int tokens) {
         return (kGroups ? 2 * kGroupBytes : kScalars + 3 * tokens * kHeadDim * 4) + kBarBytes;
     }
@@ -315,7 +315,7 @@ __device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, %0;" :
 // projections S^T k and S^T q, and once more to write Diag(exp g) S + k u^T back in place.
 __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t *stages, uint8_t *scratch, int NS,
                                                  uint32_t stage_bytes, uint64_t *full, uint64_t *done, int64_t first,
-                                                 int64_t stride, int mine) {
+                                                 int64_t stride, int mine, volatile int *s_abort) {
     using SS = StreamShape<__nv_bfloat16>;
     const int tid = threadIdx.x;
     const int grp = tid >> 7, gt = tid & 127;
@@ -354,13 +354,13 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
             slot_next = slot_of(item + 2 * stride);
             if (gt < TT) beta_next = a.beta[tok_index(item + 2 * stride, gt)];
         }
-        {  // one decision for the whole group, so that a wait that gave up in some threads only
-           // cannot split the group at its next barrier
-            const bool got = mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u);
-            if (grp == 0 ? bar_any(2, 128, !got) : bar_any(3, 128, !got)) {
-                if (!got) report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
-                break;
-            }
+        // a wait that gave up is recorded in the group's flag; the group reads the flag after
+        // its next barrier, so all of it takes the same decision (a wait that gave up in some
+        // threads only must not split the group at a barrier)
+        const bool got = mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u);
+        if (!got) {
+            report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+            s_abort[grp] = 1;
         }
         if (slot < 0) {
             for (int t = 0; t < TT; ++t) a.out[tok_index(item, t) * kHeadDim + gt] = __float2bfloat16_rn(0.0f);
@@ -371,12 +371,12 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
             continue;
         }
         uint8_t *const S = stages + (size_t)st * stage_bytes;  // bf16 [128 dk][128 dv]
+        gbar();  // the previous item's use of the group's vectors (and state slice) is over
+        if (s_abort[grp] != 0) break;  // read after the group barrier: one decision for the group
         for (int t = 0; t < TT; ++t) {
             const __nv_bfloat16 *trow =
                 reinterpret_cast<const __nv_bfloat16 *>(S + SS::kItemBytes + t * SS::kTokBytes);
-            // the previous step's use of the group's vectors (and state slice) is over; before
-            // the first token the group barrier after the stage wait has already made sure
-            if (t > 0) gbar();
+            if (t > 0) gbar();  // the previous token's use of the group's vectors is over
             {
                 const float av = __bfloat162float(trow[2 * kHeadDim + gt]);
                 s_decay[gt] = expf(gate_log_decay(av, a.gate_mode, a.lower_bound));
@@ -502,12 +502,16 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     const int64_t items = (int64_t)a.rows * H;
     const int64_t first = blockIdx.x, stride = gridDim.x;
     const int mine = items > first ? (int)((items - first + stride - 1) / stride) : 0;
+    // per compute group: a stage wait gave up (set by the threads whose wait failed, read by
+    // all after the group's next barrier)
+    volatile int *const s_abort = reinterpret_cast<volatile int *>(done + SS::kMaxStages);
     if (tid == 0) {
         for (int st = 0; st < NS; ++st) {
             mbar_init(&full[st], 1);
             mbar_init(&done[st], SS::kGroups ? kDecodeThreads / 2 : kDecodeThreads);
         }
         fence_mbar_init();
+        s_abort[0] = s_abort[1] = 0;
     }
     __syncthreads();
 
@@ -598,7 +602,8 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
 
     // ---- compute warps
     if constexpr (SS::kGroups) {
-        stream_groups_bf16(a, stages, smem + NS * stage_bytes, NS, stage_bytes, full, done, first, stride, mine);
+        stream_groups_bf16(a, stages, smem + NS * stage_bytes, NS, stage_bytes, full, done, first, stride, mine,
+                           s_abort);
         return;
     }
     const int cg = tid % VPR, rg = tid / VPR;
@@ -614,7 +619,12 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             slot_next = slot_of(item + stride);
             if (tid < TT) beta_next = a.beta[tok_index(item + stride, tid)];
         }
-        const bool got = mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u);
+        // a wait that gave up is recorded in the flag, which every compute thread reads after
+        // the next barrier (a wait that gave up in some threads only must not split them there)
+        if (!mbar_wait(&full[st], (uint32_t)(kk / NS) & 1u)) {
+            report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
+            s_abort[0] = 1;
+        }
         if (slot < 0) {
             if (tid < kHeadDim)
                 for (int t = 0; t < TT; ++t) a.out[tok_index(item, t) * kHeadDim + tid] = __float2bfloat16_rn(0.0f);
@@ -637,13 +647,9 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
         // (c mod RPP) NPASS + c / RPP, so that the NPASS rows a thread owns are contiguous.
         const __nv_bfloat16 *const rows0 =
             reinterpret_cast<const __nv_bfloat16 *>(stages + (size_t)st * stage_bytes + SS::kItemBytes);
-        // the previous item's use of the shared vectors is over; and one decision for all
-        // compute threads on the wait above (a wait that gave up in some threads only must not
-        // split them at the barriers that follow)
-        if (bar_any(1, kDecodeThreads, !got)) {
-            if (!got) report_error(a.status, KDA_ERR_DEVICE_TIMEOUT, (int)blockIdx.x);
-            break;
-        }
+        compute_bar();  // the previous item's use of the shared vectors is over
+        // read after the barrier, the flag gives all compute threads one decision
+        if (s_abort[0] != 0) break;
         for (int x = tid; x < TT * kHeadDim; x += kDecodeThreads) {
             const int t = x >> 7, c = x & (kHeadDim - 1);
             const int pc = (c % RPP) * NPASS + c / RPP;
