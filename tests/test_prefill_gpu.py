@@ -258,3 +258,24 @@ def test_bad_cu_seqlens_is_reported_not_faulted():
     st, detail = K.kda_device_status()
     assert st == K.KDA_ERR_DEVICE_INPUT and detail == 1
     assert torch.isfinite(out.float()).all()
+
+
+def test_more_than_2_31_elements_per_token_tensor():
+    """4 x 32768 tokens x H144: each token tensor holds 2.4e9 elements (> 2^31), so every token
+    and output offset needs 64 bits. The oracle checks the first and last head of every
+    sequence, whose rows sit at both ends of each tensor."""
+    lens, H = [32768] * 4, 144
+    assert sum(lens) * H * 128 > 2 ** 31
+    inp = S.prefill_inputs(lens, H, seed=29, init_std=0.02, device=DEV)
+    out, fin = K.prefill(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"], inp["cu_seqlens"],
+                         inp["init_state"], scale=SCALE, lower_bound=-5.0)
+    assert K.kda_device_status()[0] == K.KDA_OK
+    heads = [0, H - 1]
+    sub = slice_problem(inp, heads=heads)
+    ref_out, ref_fin = oracle_prefill(sub, scale=SCALE, lower_bound=-5.0, gate_mode="lower_bound")
+    assert_out_close(out[:, heads].cpu(), ref_out)
+    assert_state_close(fin[:, heads].cpu(), ref_fin)
+    # the last token of the last sequence, head H - 1, lies past element 2^31 of `out`
+    assert (sum(lens) - 1) * H * 128 + (H - 1) * 128 > 2 ** 31
+    del inp, out, fin
+    torch.cuda.empty_cache()
