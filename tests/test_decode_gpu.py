@@ -226,3 +226,30 @@ def test_multi_token_decode_equals_prefill_of_short_sequences(state_dtype, rows,
     restored = pool.clone()
     restored[sl.to(DEV)] = before[sl.to(DEV)]
     assert torch.equal(bits(restored), bits(before)), "a slot outside the live rows changed"
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,tokens", [(900, 3), (50, 8)])
+def test_multi_token_decode_with_input_options(state_dtype, rows, tokens):
+    """Several tokens per row with q/k normalised in the kernel and beta given as logits: the
+    oracle's decode applied token by token, the state carried between tokens."""
+    H = 2
+    gen = torch.Generator(device="cpu").manual_seed(60 + rows + tokens)
+    shape4 = (rows, tokens, H, 128)
+    q, k, v, g = (torch.randn(shape4, generator=gen).to(torch.bfloat16) for _ in range(4))
+    b = torch.randn(rows, tokens, H, generator=gen)
+    flags = K.KDA_DECODE_L2NORM_QK | K.KDA_DECODE_BETA_LOGITS
+    pool = S.state_pool(2048, H, state_dtype, std=0.02, seed=61, device=DEV)
+    slots = S.slot_indices(rows, 2048, seed=61, device=DEV)
+    state = pool[slots.long()].double().cpu()
+    out = torch.empty(shape4, dtype=torch.bfloat16, device=DEV)
+    K.kda_decode_ex(*(t.to(DEV) for t in (q, k, v, g, b)), slots, pool, out, SCALE, -5.0, flags=flags, norm_eps=1e-6)
+    assert K.kda_device_status()[0] == K.KDA_OK
+    outs = []
+    for t in range(tokens):
+        o, state, _ = oracle.decode(q[:, t], k[:, t], v[:, t], g[:, t], b[:, t], state, scale=SCALE, lower_bound=-5.0,
+                                    norm_eps=1e-6, beta_logits=True)
+        outs.append(o)
+    assert_out_close(out.cpu().transpose(0, 1).reshape(tokens * rows, H, 128),
+                     torch.stack([torch.as_tensor(o) for o in outs]).reshape(tokens * rows, H, 128))
+    assert_state_close(pool[slots.long()].cpu(), state)
