@@ -69,6 +69,10 @@ def parse_args(argv=None):
                         "the e2e and CPU legs are then skipped")
     p.add_argument("--no-small-bh", action="store_true",
                    help="skip the secondary 1 x 8192 H8 windowed prefill measurement")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the decode sweep (rows 1 .. 4096, FP32 and BF16 pools) reported beside the line")
+    p.add_argument("--decode-flags", default="",
+                   help="decode input options for the timed decode: comma list of l2norm, beta_logits")
     p.add_argument("--no-windows", action="store_true",
                    help="run kda_prefill (sequential chunk loop) instead of kda_prefill_ex with a workspace")
     return p.parse_args(argv)
@@ -393,13 +397,18 @@ def run_ours(args):
                          pin["init_state"], out, fin, scale, pcfg.lower_bound, pcfg.gate_mode, ws, stream,
                          checkpoints=ck, ckpt_offsets=ck_off, ckpt_every=args.ckpt_every)
 
+    dflags = decode_flags(args.decode_flags)
+    if dflags:  # the e2e and CPU legs time the plain calls
+        args.no_e2e = args.no_cpu_baseline = True
+
     def decode_call():
-        if T == 1:
+        if T == 1 and not dflags:
             K.kda_decode(din["q"], din["k"], din["v"], din["g_raw"], din["beta"], din["slot_idx"], pool, dout,
                          dcfg.scale, dcfg.lower_bound, dcfg.gate_mode, stream)
         else:
             K.kda_decode_ex(din["q"], din["k"], din["v"], din["g_raw"], din["beta"], din["slot_idx"], pool, dout,
-                            dcfg.scale, dcfg.lower_bound, dcfg.gate_mode, stream=stream)
+                            dcfg.scale, dcfg.lower_bound, dcfg.gate_mode, flags=dflags, norm_eps=1e-6,
+                            stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -445,6 +454,9 @@ def run_ours(args):
     small = None
     if not args.no_small_bh and not args.seqlens and not args.heads and args.prefill != "prefill_h8_t8192":
         small = measure_small_bh(K, args, device, rank, flush, stream, dist, peaks, peak_src, traffic, sms)
+    sweep = None
+    if not args.no_sweep and not args.pool_slots and T == 1 and not dflags:
+        sweep = measure_decode_sweep(K, args, device, rank, flush, stream, dist, peaks, pool)
 
     e2e = None if args.no_e2e else measure_e2e(K, pcfg, pin, dcfg, din, pool, stream, device, args, dist, ws)
     cpu = None
@@ -494,7 +506,8 @@ def run_ours(args):
                                "heads": pcfg.num_heads, "gate": pcfg.gate_mode, "lower_bound": pcfg.lower_bound,
                                "init_state": pcfg.init_std is not None, "ckpt_every": args.ckpt_every},
                    "decode": {"rows": args.decode_rows, "heads": dcfg.num_heads, "pool_slots": dcfg.num_slots,
-                              "state_dtype": args.state_dtype, "tokens_per_row": T},
+                              "state_dtype": args.state_dtype, "tokens_per_row": T,
+                              "options": args.decode_flags or "none"},
                    "precision": "bf16 operands, tf32 state update, fp32 state and accumulation",
                    "prefill_schedule": schedule_name(ws, full_waves, chains, sms),
                    "l2": f"flushed between steps ({flush.numel() >> 20} MiB write)",
@@ -514,6 +527,8 @@ def run_ours(args):
     }
     if small is not None:
         line["prefill_small_bh"] = small
+    if sweep is not None:
+        line["decode_sweep"] = sweep
     if sampler:
         line["clocks"] = sampler.summary()
     if e2e is not None:
@@ -523,6 +538,63 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+def decode_flags(text):
+    """KDA_DECODE_* bits from a comma list of option names."""
+    names = {"l2norm": 1, "beta_logits": 2}
+    bits = 0
+    for name in filter(None, (x.strip() for x in text.split(","))):
+        if name not in names:
+            raise SystemExit(f"--decode-flags: unknown option {name!r} (l2norm, beta_logits)")
+        bits |= names[name]
+    return bits
+
+
+def measure_decode_sweep(K, args, device, rank, flush, stream, dist, peaks, pool_f32):
+    """The whole decode workload: rows 1, 2, 4 .. 4096 x H8 on 16384-slot FP32 and BF16 pools,
+    each row count timed over --steps calls (L2 flushed between them). Reports per row count the
+    median time in microseconds and the fraction of HBM bandwidth on the state and token bytes."""
+    import torch
+
+    import kda_synth as S
+    cfg = S.configs()["decode_h8_pool16384"]
+    H = cfg.num_heads
+    res = {}
+    for dt in ("f32", "bf16"):
+        pool = pool_f32 if (dt == "f32" and args.state_dtype == "f32") else \
+            S.state_pool(cfg.num_slots, H, dt, std=cfg.pool_std, seed=rank_seed(cfg.seed, rank), device=device)
+        us, frac = [], []
+        for rows in cfg.rows:
+            d = S.decode_inputs(rows, H, seed=rank_seed(cfg.seed, rank) + rows, device=device)
+            slots = S.slot_indices(rows, cfg.num_slots, seed=rank_seed(cfg.seed, rank), device=device)
+            out = torch.empty_like(d["q"])
+
+            def call():
+                K.kda_decode(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], slots, pool, out, cfg.scale,
+                             cfg.lower_bound, cfg.gate_mode, stream)
+
+            for _ in range(2):
+                call()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for a_, b_ in ev:
+                flush.zero_()
+                a_.record(stream)
+                call()
+                b_.record(stream)
+            torch.cuda.synchronize(device)
+            ms = max_over_ranks(statistics.median(a_.elapsed_time(b_) for a_, b_ in ev), dist, device)
+            us.append(round(ms * 1e3, 2))
+            frac.append(round(decode_bytes(rows, H, dt) / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4))
+        res[dt] = {"us_median": us, "hbm_frac": frac}
+        if pool is not pool_f32:
+            del pool
+    st, detail = K.kda_device_status()
+    if st != K.KDA_OK:
+        raise RuntimeError(f"device status {st} ({detail}) after the decode sweep")
+    return {"rows": list(cfg.rows), "heads": H, "pool_slots": cfg.num_slots, **res,
+            "timing": "CUDA events per call, L2 flushed between calls, median of --steps calls"}
 
 
 def measure_small_bh(K, args, device, rank, flush, stream, dist, peaks, peak_src, traffic, sms):

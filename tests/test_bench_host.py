@@ -62,3 +62,11 @@ def test_traffic_record_matches_the_kernel_sources():
             assert bench.scaled_traffic(t, name, 10) == pytest.approx(10 * rec["dram_bytes_per_unit"], rel=1e-6)
         else:
             assert bench.scaled_traffic(t, name, 10) is None
+
+
+def test_decode_flag_names():
+    assert bench.decode_flags("") == 0
+    assert bench.decode_flags("l2norm") == 1
+    assert bench.decode_flags("beta_logits, l2norm") == 3
+    with pytest.raises(SystemExit):
+        bench.decode_flags("l2norm,unknown")
