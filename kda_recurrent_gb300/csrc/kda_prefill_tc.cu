@@ -155,10 +155,6 @@ __device__ __forceinline__ float bfv(const uint8_t *base, int elem) {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[elem]);
 }
 
-__device__ __forceinline__ void st_bf16(uint8_t *base, int elem, float x) {
-    reinterpret_cast<__nv_bfloat16 *>(base)[elem] = __float2bfloat16_rn(x);
-}
-
 // Byte offset of element (row, col) of a K-major tf32 operand tile made of 8-row x
 // 16-byte core matrices; `sbo` = bytes per 8-row group (rows are N, cols are K).
 __device__ __forceinline__ int core_off_tf32(int row, int col, int sbo) {
@@ -195,11 +191,6 @@ __device__ __forceinline__ float gate_decay_m(float av, float lb2) {
     return ex2(av * kLog2e);
 }
 
-__device__ __forceinline__ void unpack_bf16x2(uint32_t w, float &lo, float &hi) {
-    lo = __uint_as_float(w << 16);
-    hi = __uint_as_float(w & 0xffff0000u);
-}
-
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
@@ -226,10 +217,6 @@ __device__ __forceinline__ float2 gate_decay2(float2 av, float lb2) {
         return make_float2(rcp(den.x), rcp(den.y));
     }
     return make_float2(ex2(e.x), ex2(e.y));
-}
-
-__device__ __forceinline__ void st_pair(uint8_t *base, int elem, float lo, float hi) {
-    *reinterpret_cast<uint32_t *>(base + 2 * elem) = pack_bf16(lo, hi);
 }
 
 __device__ __forceinline__ void st_pair(uint8_t *base, int elem, float2 v) {
@@ -326,25 +313,35 @@ __device__ __forceinline__ void v_to_tmem(uint32_t tmem, const uint8_t *rv, int 
     tmem_wait_st();
 }
 
-// One 16 x 16 block of the pair products by one warp (mma.sync m16n8k16, BF16, FP32
-// accumulate): `which` 0 is Mqk (query rows), 1 is N = Diag(beta) A (key rows); block 0 and 1
-// are the diagonal blocks of the two halves, 2 the off-diagonal one. Mqk is stored row-major
-// with the causal mask, N transposed and strictly lower.
-__device__ __forceinline__ void pair_block(const uint8_t *smem, int which, int blk, int lane, const float *rb,
-                                           float *mq_s, float *nt_s) {
+// One 16 x 16 block of both pair products by one warp (mma.sync m16n8k16, BF16, FP32
+// accumulate), in a single pass over k: N = Diag(beta) A (key rows) and, unless kKeysOnly, Mqk
+// (query rows). Block 0 and 1 are the diagonal blocks of the two halves, 2 the off-diagonal
+// one. The two products share their right operand (the key columns), so each k step loads it
+// once, and the four accumulators give the warp four independent mma.sync chains. Mqk is
+// stored row-major with the causal mask, N transposed and strictly lower.
+template <bool kKeysOnly>
+__device__ __forceinline__ void pair_blocks_nq(const uint8_t *smem, int blk, int lane, const float *rb, float *mq_s,
+                                               float *nt_s) {
     const int g = lane >> 2, t4 = lane & 3;
-    const uint8_t *Lb = smem + (which ? kPairKL : kPairQ);
-    const uint8_t *Rb = smem + kPairKR;
+    const uint8_t *const Kl = smem + kPairKL;
+    const uint8_t *const Ql = smem + kPairQ;
+    const uint8_t *const Rb = smem + kPairKR;
     const int row0 = 16 * blk;
-    float acc[2][4] = {};
+    float an[2][4] = {}, aq[2][4] = {};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4], bfr[4];
-        ldsm_x4(af, smem_addr(Lb + ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2));
+        uint32_t fk[4], fq[4], bfr[4];
+        const int aoff = ((row0 + (lane & 15)) * kRowB + 16 * ks + (lane >> 4) * 8) * 2;
+        ldsm_x4(fk, smem_addr(Kl + aoff));
+        if (!kKeysOnly) ldsm_x4(fq, smem_addr(Ql + aoff));
         ldsm_x4(bfr, smem_addr(Rb + ((row0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + 16 * ks +
                                      ((lane >> 3) & 1) * 8) * 2));
-        mma_bf16_16816(acc[0], af, bfr[0], bfr[1]);
-        mma_bf16_16816(acc[1], af, bfr[2], bfr[3]);
+        mma_bf16_16816(an[0], fk, bfr[0], bfr[1]);
+        mma_bf16_16816(an[1], fk, bfr[2], bfr[3]);
+        if (!kKeysOnly) {
+            mma_bf16_16816(aq[0], fq, bfr[0], bfr[1]);
+            mma_bf16_16816(aq[1], fq, bfr[2], bfr[3]);
+        }
     }
     const int oi = (blk == 0) ? 0 : 16;
     const int oj = (blk == 1) ? 16 : 0;
@@ -354,11 +351,8 @@ __device__ __forceinline__ void pair_block(const uint8_t *smem, int which, int b
         for (int e = 0; e < 4; ++e) {
             const int i = oi + g + 8 * (e >> 1);
             const int j = oj + 8 * nt + 2 * t4 + (e & 1);
-            const float val = acc[nt][e];
-            if (which == 0)
-                mq_s[i * kSq + j] = (j <= i) ? val : 0.0f;
-            else
-                nt_s[j * kSq + i] = (j < i) ? val * rb[i] : 0.0f;
+            nt_s[j * kSq + i] = (j < i) ? an[nt][e] * rb[i] : 0.0f;
+            if (!kKeysOnly) mq_s[i * kSq + j] = (j <= i) ? aq[nt][e] : 0.0f;
         }
     }
 }
@@ -624,12 +618,9 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         }
         tc_fence_after();
         // ---- pair products: warp w takes N block w (the diagonal ones are inverted at once by
-        //      the same warp) and then Mqk block w; warp 3 zeroes the blocks above the diagonal.
+        //      the same warp) together with Mqk block w; warp 3 zeroes the blocks above the diagonal.
         //      Then V^T into D1 and beta aside, after which group A may refill what was read.
-        if (bwarp < 3) {
-            pair_block(smem, 1, bwarp, lane, rb, mq_s, nt_s);
-            if (!kPass1) pair_block(smem, 0, bwarp, lane, rb, mq_s, nt_s);
-        }
+        if (bwarp < 3) pair_blocks_nq<kPass1>(smem, bwarp, lane, rb, mq_s, nt_s);
         mbar_arrive(&B->ab_empty);  // this thread's reads of the pair operands are done
         if (bwarp < 2) {
             __syncwarp();
