@@ -13,11 +13,12 @@
 //     D1^T += S^T [-Kbar; Qbar]^T   M128 N64 K128, kind::tf32, A = S^T read from TMEM
 //                                   -> D1^T = [R^T | (Qbar S)^T]
 //     D1^T[:, 32:64] += R^T Bo^T    M128 N32 K32,  A = R^T read from TMEM      -> O^T
-//     S_nxt = S_cur Diag(2^G_last)                                  (state warps, TMEM -> TMEM)
-//     S_nxt^T += R^T Kt             M128 N128 K32, A = R^T read from TMEM
+//     S = S Diag(2^G_last)                       (state warps, in TMEM, after the projection)
+//     S^T += R^T Kt                 M128 N128 K32, A = R^T read from TMEM
 // Kt^T = Kr^T T' is one more small tcgen05 product (M128 N32 K32, both operands in shared
-// memory, TF32), issued by the producers off the serial chain. The state is ping-ponged between two TMEM buffers so that
-// the decay runs while the projection reads the previous buffer.
+// memory, TF32), issued by the producers off the serial chain. The decay runs in place once the
+// projection has read the state: run beside the projection, the two shared the tensor memory's
+// bandwidth and the projection took several times its tensor-core time.
 //
 // Warp roles (one CTA per (sequence, head) chain, 16 warps), a chunk per group in flight:
 //   warps 0-7   group A: raw loads (cp.async), gate and decay products, the pair operands
@@ -106,7 +107,7 @@ static_assert(kSmemLaunch <= 227 * 1024, "one CTA per SM");
 
 // ---- tensor-memory map (columns; 512 allocated)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;     // S^T ping-pong: [0,128) and [128,256)
+constexpr uint32_t kColS = 0;     // S^T [0,128) (the window pass keeps M^T at [128,256))
 constexpr uint32_t kColD1 = 256;  // D1 double buffer: [256,320) and [320,384)
 constexpr uint32_t kColKt = 384;  // Kt^T (lane = dk, column = token), producer-owned
 
@@ -819,7 +820,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
     bool alive = true;
     for (int c = 0; c < nchunks && alive; ++c) {
         const int ps = c & 1, db = c & 1;
-        const uint32_t cur = kColS + 128 * (c & 1), nxt = kColS + 128 * ((c + 1) & 1);
+        const uint32_t cur = kColS;  // the state stays in one buffer, decayed in place
         const uint8_t *stage = smem + kStage0 + ps * kStageBytes;
         if (!wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status)) break;
         if (c >= 1 && !wait_or_abort(&B->g2, (c - 1) & 1, B, a.status)) break;
@@ -839,16 +840,20 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                 store_state(tmem + cur, lane_base, dv,
                             a.ckpt + ((size_t)row * a.num_heads + h) * (kHeadDim * kHeadDim));
         }
-        // decay into the other state buffer while the projection reads this one
-        decay_columns(tmem + lane_base + cur, tmem + lane_base + nxt, reinterpret_cast<const float *>(stage + kStDec),
-                      4);
+        // the decay in place, once the projection has read the state (running it beside the
+        // projection made both share the tensor memory's bandwidth)
+        const bool lost = !wait_or_abort(&B->g1, c & 1, B, a.status);
+        tc_fence_after();
+        if (!lost)
+            decay_columns(tmem + lane_base + cur, tmem + lane_base + cur,
+                          reinterpret_cast<const float *>(stage + kStDec), 4);
         tc_fence_before();
-        bar_named(kBarState, kStateThreads);
+        if (bar_any(kBarState, kStateThreads, lost)) break;
         tc_fence_after();
         if (mma_thread) {
-            if (wait_or_abort(&B->g1, c & 1, B, a.status)) {
-                tc_fence_after();
-                // O^T = (Qbar S)^T + R^T Bo^T, then S_nxt^T += R^T Kt (A = R^T = D1^T[:, 0:32])
+            {
+                // O^T = (Qbar S)^T + R^T Bo^T, then S^T += R^T Kt on the decayed state
+                // (A = R^T = D1^T[:, 0:32])
                 const uint32_t obase = smem_addr(stage + kStBo);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
@@ -858,7 +863,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                 const uint32_t kbase = smem_addr(stage + kStKt);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_tf32_ts(tmem + nxt, tmem + kColD1 + 64 * db + 8 * s,
+                    mma_tf32_ts(tmem + cur, tmem + kColD1 + 64 * db + 8 * s,
                                 smem_desc_kmajor(kbase + 256 * s, 128, 1024), kIdescG2, true);
                 mma_commit(&B->g2);
                 mma_commit(&B->g2s[ps]);
@@ -911,11 +916,11 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
             const bool full = bos + kChunk * nchunks <= eos;
             const int64_t row = checkpoint_row(a, n, chunk_base + nchunks - 1, full);
             if (row >= 0)
-                store_state(tmem + kColS + 128 * (nchunks & 1), lane_base, dv,
+                store_state(tmem + kColS, lane_base, dv,
                             a.ckpt + ((size_t)row * a.num_heads + h) * (kHeadDim * kHeadDim));
         }
         if (fin_out != nullptr) {
-            const uint32_t fin = kColS + 128 * (nchunks & 1);
+            const uint32_t fin = kColS;
 #pragma unroll 1
             for (int j = 0; j < 8; ++j) {
                 float v[16];
