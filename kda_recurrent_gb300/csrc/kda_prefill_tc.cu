@@ -28,7 +28,8 @@
 //               (I + Diag(beta) A)^-1 in FP32 by 16 x 16 blocks, T', the Kt MMA (tcgen05),
 //               Bo (mma.sync, TF32) and the hand-off of the stage;
 //   warps 12-15 state warps (one per TMEM lane quadrant): initial/final state, the decay,
-//               the output read-out and store; lane 0 of warp 12 issues the state MMAs.
+//               the output read-out and store; lane 0 of warps 12 and 13 issue the state
+//               MMAs, as two streams of independent accumulators.
 // Two stages of operands are in flight; the pair operands, the raw v and beta buffers and
 // TMEM's D1 buffers are each released as soon as their reader is done with them.
 // Exponent range: per 16-token half, factors are anchored at the half's 8th token, built
@@ -128,7 +129,7 @@ struct Bars {
     uint64_t ab_empty;   // group B -> A: the pair operands of a chunk consumed
                          //   (count kSolveThreads, one phase per chunk)
     uint64_t vfree;      // group B -> A: the raw v, beta of a chunk consumed (same counting)
-    uint64_t drain;      // after an abort: the two MMA-issuing threads' work complete (count 2)
+    uint64_t drain;      // after an abort: the three MMA-issuing threads' work complete (count 3)
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -802,6 +803,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
     const int dv = 32 * quad + lane;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const bool mma_thread = (warp == kFirstStateWarp) && (lane == 0);
+    const bool mma_thread2 = (warp == kFirstStateWarp + 1) && (lane == 0);  // a second MMA stream
 
     // initial state -> S^T buffer 0 (lane = dv, column = dk)
 #pragma unroll 1
@@ -850,24 +852,24 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         tc_fence_before();
         if (bar_any(kBarState, kStateThreads, lost)) break;
         tc_fence_after();
+        // O^T = (Qbar S)^T + R^T Bo^T and S^T += R^T Kt on the decayed state (A = R^T =
+        // D1^T[:, 0:32]): different accumulators, issued from two warps so that the two MMA
+        // streams go in parallel (one thread issues a tcgen05.mma only every ~90 cycles)
         if (mma_thread) {
-            {
-                // O^T = (Qbar S)^T + R^T Bo^T, then S^T += R^T Kt on the decayed state
-                // (A = R^T = D1^T[:, 0:32])
-                const uint32_t obase = smem_addr(stage + kStBo);
+            const uint32_t obase = smem_addr(stage + kStBo);
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_tf32_ts(tmem + kColD1 + 64 * db + 32, tmem + kColD1 + 64 * db + 8 * s,
-                                smem_desc_kmajor(obase + 256 * s, 128, 1024), kIdescN32, true);
-                mma_commit(&B->go);
-                const uint32_t kbase = smem_addr(stage + kStKt);
+            for (int s = 0; s < 4; ++s)
+                mma_tf32_ts(tmem + kColD1 + 64 * db + 32, tmem + kColD1 + 64 * db + 8 * s,
+                            smem_desc_kmajor(obase + 256 * s, 128, 1024), kIdescN32, true);
+            mma_commit(&B->go);
+        } else if (mma_thread2) {
+            const uint32_t kbase = smem_addr(stage + kStKt);
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_tf32_ts(tmem + cur, tmem + kColD1 + 64 * db + 8 * s,
-                                smem_desc_kmajor(kbase + 256 * s, 128, 1024), kIdescG2, true);
-                mma_commit(&B->g2);
-                mma_commit(&B->g2s[ps]);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_tf32_ts(tmem + cur, tmem + kColD1 + 64 * db + 8 * s,
+                            smem_desc_kmajor(kbase + 256 * s, 128, 1024), kIdescG2, true);
+            mma_commit(&B->g2);
+            mma_commit(&B->g2s[ps]);
         }
         __syncwarp();
         // output read-out: O^T = D1^T[:, 32:64]
@@ -949,6 +951,7 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
     const int row = 32 * quad + lane;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const bool mma_thread = (warp == kFirstStateWarp) && (lane == 0);
+    const bool mma_thread2 = (warp == kFirstStateWarp + 1) && (lane == 0);  // a second MMA stream
 
 #pragma unroll 1
     for (int j = 0; j < 8; ++j) {
@@ -972,13 +975,16 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         if (!wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status)) break;
         if (c >= 1 && !wait_or_abort(&B->g2, (c - 1) & 1, B, a.status)) break;
         tc_fence_after();
-        if (mma_thread) {
+        // the S chain and the M chain from two warps, in parallel (both commit g1)
+        if (mma_thread || mma_thread2) {
             const uint32_t wbase = smem_addr(stage + kStW);
+            const uint32_t d = mma_thread ? kColD1 + 32 * db : kColD1M + 32 * db;
+            const uint32_t src = mma_thread ? kColS : kColM;
 #pragma unroll
             for (int s = 0; s < 16; ++s) {
                 const uint64_t bd = smem_desc_sw128(wbase + (s >> 2) * 8192 + (s & 3) * 32);
-                mma_tf32_ts(tmem + kColD1 + 32 * db, tmem + kColS + 8 * s, bd, kIdescN32, true);
-                mma_tf32_ts(tmem + kColD1M + 32 * db, tmem + kColM + 8 * s, bd, kIdescN32, s > 0);
+                // D1 for S starts from V; D1 for M from zero
+                mma_tf32_ts(tmem + d, tmem + src + 8 * s, bd, kIdescN32, mma_thread || s > 0);
             }
             mma_commit(&B->g1);
         }
@@ -992,14 +998,13 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         mbar_arrive(&B->oread[db]);
         bar_named(kBarState, kStateThreads);
         tc_fence_after();
-        if (mma_thread) {
+        if (mma_thread || mma_thread2) {  // both commit g2 and g2s
             const uint32_t kbase = smem_addr(stage + kStKt);
+            const uint32_t d = mma_thread ? kColS : kColM;
+            const uint32_t r = mma_thread ? kColD1 + 32 * db : kColD1M + 32 * db;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t bd = smem_desc_kmajor(kbase + 256 * s, 128, 1024);
-                mma_tf32_ts(tmem + kColS, tmem + kColD1 + 32 * db + 8 * s, bd, kIdescG2, true);
-                mma_tf32_ts(tmem + kColM, tmem + kColD1M + 32 * db + 8 * s, bd, kIdescG2, true);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_tf32_ts(tmem + d, tmem + r + 8 * s, smem_desc_kmajor(kbase + 256 * s, 128, 1024), kIdescG2, true);
             mma_commit(&B->g2);
             mma_commit(&B->g2s[ps]);
         }
@@ -1150,15 +1155,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         mbar_init(&B->ab_full[1], kProdThreads);
         mbar_init(&B->ab_empty, kSolveThreads);
         mbar_init(&B->vfree, kSolveThreads);
-        mbar_init(&B->g1, 1);
+        // the window pass's S and M chains are issued by two threads, which both commit
+        mbar_init(&B->g1, kPass1 ? 2 : 1);
         mbar_init(&B->go, 1);
         mbar_init(&B->kt, 1);
-        mbar_init(&B->g2, 1);
-        mbar_init(&B->g2s[0], 1);
-        mbar_init(&B->g2s[1], 1);
+        mbar_init(&B->g2, kPass1 ? 2 : 1);
+        mbar_init(&B->g2s[0], kPass1 ? 2 : 1);
+        mbar_init(&B->g2s[1], kPass1 ? 2 : 1);
         mbar_init(&B->oread[0], kStateThreads);
         mbar_init(&B->oread[1], kStateThreads);
-        mbar_init(&B->drain, 2);
+        mbar_init(&B->drain, 3);
         B->abort = 0;
         fence_mbar_init();
     }
@@ -1195,9 +1201,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     __syncthreads();
     tc_fence_after();
     // After an abort (every group has left its loop, so all threads read the same flag), the
-    // two threads that issue MMAs drain whatever they still have in flight before the tensor
-    // memory is released; the wait is bounded like every other.
-    if (B->abort != 0 && (threadIdx.x == kKtThread || threadIdx.x == kFirstStateWarp * 32)) {
+    // three threads that issue MMAs (group B's Kt thread and the state warps' two) drain
+    // whatever they still have in flight before the tensor memory is released; the wait is
+    // bounded like every other.
+    if (B->abort != 0 && (threadIdx.x == kKtThread || threadIdx.x == kFirstStateWarp * 32 ||
+                          threadIdx.x == (kFirstStateWarp + 1) * 32)) {
         mma_commit(&B->drain);
         mbar_wait(&B->drain, 0);
         tc_fence_before();
