@@ -82,8 +82,12 @@ constexpr int kRawBeta = kRawV + 2 * kRawVBytes;  // fp32 [2][32]: beta, one buf
 constexpr int kStage0 = (kRawBeta + 256 + 1023) / 1024 * 1024;  // 1024-aligned (swizzle atoms)
 // One stage per chunk in flight: the operands the state MMAs read.
 constexpr int kStW = 0;                           // tf32 [4 K-atoms][64 tok][32 dk], 128-byte swizzle
+// Kr / Kt: 8-row groups 1040 bytes apart instead of 1024, so that rows r and r + 8 fall in
+// different 16-byte bank groups: the operand warps store rows 2p and 2p + 1 for channel pairs p,
+// and a quarter warp's 8 float4 stores (rows 0, 2, ..., 14) then hit all 8 bank groups
+constexpr int kKtSbo = 1040;
 constexpr int kStKt = kStW + 4 * 8192;            // tf32 [128 dk][32 tok]: Kr, then Kt in place
-constexpr int kStBo = kStKt + 16384;              // tf32 [32 tok][32 tok]: Bo = Mqk T'
+constexpr int kStBo = kStKt + 16 * kKtSbo;        // tf32 [32 tok][32 tok]: Bo = Mqk T'
 constexpr int kStDec = kStBo + 4096;              // fp32 [128]: 2^G_last
 constexpr int kStageBytes = (kStDec + 512 + 1023) / 1024 * 1024;
 constexpr int kOst = kStage0 + 2 * kStageBytes;   // bf16x2 [16][128]: output staging (tokens t, 16 + t)
@@ -285,7 +289,7 @@ __device__ __forceinline__ void kt_to_stage(uint32_t tmem, uint8_t *stage, int b
         tmem_wait_ld();
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4)
-            *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(dk, 16 * half + 4 * e4, 1024)) =
+            *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(dk, 16 * half + 4 * e4, kKtSbo)) =
                 make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
     }
 }
@@ -564,9 +568,9 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
 #pragma unroll
             for (int h4 = 0; h4 < 2; ++h4) {
                 const int i0 = 8 * qt + 4 * h4;
-                *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch, i0, 1024)) =
+                *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch, i0, kKtSbo)) =
                     make_float4(kr[4 * h4].x, kr[4 * h4 + 1].x, kr[4 * h4 + 2].x, kr[4 * h4 + 3].x);
-                *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch + 1, i0, 1024)) =
+                *reinterpret_cast<float4 *>(stage + kStKt + core_off_tf32(ch + 1, i0, kKtSbo)) =
                     make_float4(kr[4 * h4].y, kr[4 * h4 + 1].y, kr[4 * h4 + 2].y, kr[4 * h4 + 3].y);
             }
             if (qt == 0)
@@ -687,7 +691,7 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
             const uint32_t kra = smem_addr(stage + kStKt), ah = smem_addr(at_hi);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_tf32_ss(tmem + kColKt, smem_desc_kmajor(kra + 256 * s, 128, 1024),
+                mma_tf32_ss(tmem + kColKt, smem_desc_kmajor(kra + 256 * s, 128, kKtSbo),
                             smem_desc_kmajor(ah + 256 * s, 128, 1024), kIdescN32, s > 0);
 
             mma_commit(&B->kt);
@@ -867,7 +871,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_tf32_ts(tmem + cur, tmem + kColD1 + 64 * db + 8 * s,
-                            smem_desc_kmajor(kbase + 256 * s, 128, 1024), kIdescG2, true);
+                            smem_desc_kmajor(kbase + 256 * s, 128, kKtSbo), kIdescG2, true);
             mma_commit(&B->g2);
             mma_commit(&B->g2s[ps]);
         }
@@ -884,10 +888,13 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         mbar_arrive(&B->oread[db]);
         // staged through shared memory for 16-byte row stores; the buffer is reused by the
         // next chunk only after the barrier that closes this iteration
-        // tokens t and 16 + t share a 32-bit word: ost[t][dv] = bf16x2(O[t][dv], O[16 + t][dv])
+        // tokens t and 16 + t share a 32-bit word: ost[t][dv] = bf16x2(O[t][dv], O[16 + t][dv]),
+        // with the two 16-byte halves of each 32-byte group swapped where dv bit 5 is set, so
+        // that a quarter warp's 16-byte reads below (32 bytes apart) hit all 8 bank groups
         uint32_t *const ost = reinterpret_cast<uint32_t *>(smem + kOst);
+        const int dvs = dv ^ (((dv >> 5) & 1) << 2);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) ost[t * kHeadDim + dv] = pack_bf16(o0[t], o1[t]);
+        for (int t = 0; t < 16; ++t) ost[t * kHeadDim + dvs] = pack_bf16(o0[t], o1[t]);
         bar_named(kBarState, kStateThreads);
         const int t0 = bos + kChunk * c;
         const int L = min(kChunk, eos - t0);
@@ -895,8 +902,9 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         for (int m = 0; m < 2; ++m) {
             const int idx = stid + kStateThreads * m;
             const int t = idx >> 4, vec = idx & 15;
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(ost + t * kHeadDim + vec * 8);
-            const uint4 w1 = *reinterpret_cast<const uint4 *>(ost + t * kHeadDim + vec * 8 + 4);
+            const int sw = 4 * ((vec >> 2) & 1);  // where dv = 8 vec .. 8 vec + 3 was stored
+            const uint4 w0 = *reinterpret_cast<const uint4 *>(ost + t * kHeadDim + vec * 8 + sw);
+            const uint4 w1 = *reinterpret_cast<const uint4 *>(ost + t * kHeadDim + vec * 8 + (4 - sw));
             __nv_bfloat16 *const orow = a.out + ((size_t)(t0 + t) * a.num_heads + h) * kHeadDim + vec * 8;
             if (t < L)
                 *reinterpret_cast<uint4 *>(orow) =
@@ -1004,7 +1012,7 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
             const uint32_t r = mma_thread ? kColD1 + 32 * db : kColD1M + 32 * db;
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_tf32_ts(tmem + d, tmem + r + 8 * s, smem_desc_kmajor(kbase + 256 * s, 128, 1024), kIdescG2, true);
+                mma_tf32_ts(tmem + d, tmem + r + 8 * s, smem_desc_kmajor(kbase + 256 * s, 128, kKtSbo), kIdescG2, true);
             mma_commit(&B->g2);
             mma_commit(&B->g2s[ps]);
         }
