@@ -667,6 +667,8 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
             if ((tid & 31) == 0) s_ts[t] = make_float4(x.qk, x.rq, x.rk, 0.0f);
         }
         compute_bar();
+        __nv_bfloat16 *const out_row = a.out + tok_index(item, 0) * kHeadDim;  // token t at t * out_tok_stride
+        const size_t out_tok_stride = (size_t)H * kHeadDim;
         for (int t = 0; t < TT; ++t) {
             const __nv_bfloat16 *trow = rows0 + t * (SS::kTokBytes / 2);
             const float *const s_decay = s_vec + t * 3 * kHeadDim;
@@ -713,18 +715,24 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
                     __fmul2_rn(wq[e], make_float2(ts.rq, ts.rq));
             }
             compute_bar();
-            if (tid < kHeadDim) {
-                float w_k = 0.0f, w_q = 0.0f;
-#pragma unroll 8
-                for (int i = 0; i < RPP; ++i) {
-                    w_k += s_red[(0 * RPP + i) * kHeadDim + tid];
-                    w_q += s_red[(1 * RPP + i) * kHeadDim + tid];
-                }
-                const float u = beta_of(s_beta[t], a) * (__bfloat162float(trow[3 * kHeadDim + tid]) - w_k);
-                s_u[tid] = u;
-                a.out[tok_index(item, t) * kHeadDim + tid] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, u, w_q));
+            // the column sums by all compute threads: thread c < 128 sums (S^T k)_c and forms u_c,
+            // thread 128 + c sums (S^T q)_c and forms the output once u is published
+            float w;
+            {
+                const float *const src = s_red + (tid >> 7) * RPP * kHeadDim + (tid & (kHeadDim - 1));
+                float x[RPP];
+#pragma unroll
+                for (int i = 0; i < RPP; ++i) x[i] = src[i * kHeadDim];
+                w = x[0];
+#pragma unroll
+                for (int i = 1; i < RPP; ++i) w += x[i];
             }
+            if (tid < kHeadDim) s_u[tid] = beta_of(s_beta[t], a) * (__bfloat162float(trow[3 * kHeadDim + tid]) - w);
             compute_bar();
+            if (tid >= kHeadDim) {
+                const int c = tid - kHeadDim;
+                out_row[t * out_tok_stride + c] = __float2bfloat16_rn(a.scale * fmaf(ts.qk, s_u[c], w));
+            }
             float2 uv[VEC / 2];
 #pragma unroll
             for (int e = 0; e < VEC / 2; ++e) uv[e] = *reinterpret_cast<const float2 *>(&s_u[cg * VEC + 2 * e]);

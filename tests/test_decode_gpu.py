@@ -253,3 +253,55 @@ def test_multi_token_decode_with_input_options(state_dtype, rows, tokens):
     assert_out_close(out.cpu().transpose(0, 1).reshape(tokens * rows, H, 128),
                      torch.stack([torch.as_tensor(o) for o in outs]).reshape(tokens * rows, H, 128))
     assert_state_close(pool[slots.long()].cpu(), state)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("gate_mode", ["lower_bound", "softplus", "log_decay"])
+def test_multi_token_decode_extreme_gates(state_dtype, gate_mode):
+    """16 tokens per row with gates whose per-channel decay products leave [2^-60, 2^60] within
+    the row, so that a kernel that defers the decay to the end of the row has to fold it into
+    the state mid-row: lower bound -8 with saturated gates (a decay product below 2^-60 after 6
+    tokens); softplus gates of 60 (e^-60 in one token) and 200 (a decay that underflows FP32);
+    log-decay gates alternating +45 / -45 on channels whose k and q are zero (the row grows
+    past 2^60 and shrinks back without reaching any output). The oracle's decode applied token
+    by token, in FP64."""
+    H, rows, tokens = 4, 300, 16
+    gen = torch.Generator(device="cpu").manual_seed(70)
+    shape4 = (rows, tokens, H, 128)
+    q, k, v = (torch.randn(shape4, generator=gen) for _ in range(3))
+    g = torch.randn(shape4, generator=gen)
+    lb = 0.0
+    if gate_mode == "lower_bound":
+        lb = -8.0
+        g[..., :64] = 8.0
+    elif gate_mode == "softplus":
+        g[:, 2::5, :, :32] = 60.0
+        g[:, 3::7, :, 32:40] = 200.0
+    else:
+        g = -0.3 * g.abs()
+        sign = torch.tensor([45.0 if t % 2 == 0 else -45.0 for t in range(tokens)])
+        g[..., 100:104] = sign.view(1, tokens, 1, 1)
+        q[..., 100:104] = 0.0
+        k[..., 100:104] = 0.0
+    # unit q and k per token (zero rows stay zero), as the model's normalised projections
+    q, k = (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-6) for x in (q, k))
+    q, k, v, g = (t.to(torch.bfloat16) for t in (q, k, v, g))
+    b = torch.rand(rows, tokens, H, generator=gen)
+    pool = S.state_pool(1024, H, state_dtype, std=0.02, seed=71, device=DEV)
+    slots = S.slot_indices(rows, 1024, seed=71, device=DEV)
+    state = pool[slots.long()].double().cpu()
+    out = torch.empty(shape4, dtype=torch.bfloat16, device=DEV)
+    K.kda_decode_ex(*(t.to(DEV) for t in (q, k, v, g, b)), slots, pool, out, SCALE, lb, gate_mode=gate_mode)
+    assert K.kda_device_status()[0] == K.KDA_OK
+    outs = []
+    for t in range(tokens):
+        o, state, _ = oracle.decode(q[:, t], k[:, t], v[:, t], g[:, t], b[:, t], state, scale=SCALE, lower_bound=lb,
+                                    gate_mode=gate_mode)
+        if state_dtype == "bf16":
+            # a BF16 pool is rounded on every store of the state, and the kernel stores it after
+            # every token: the row's tokens act as that many one-token steps on the BF16 state
+            state = torch.as_tensor(state).to(torch.bfloat16).to(torch.float64).numpy()
+        outs.append(o)
+    assert_out_close(out.cpu().transpose(0, 1).reshape(tokens * rows, H, 128),
+                     torch.stack([torch.as_tensor(o) for o in outs]).reshape(tokens * rows, H, 128))
+    assert_state_close(pool[slots.long()].cpu(), state)
