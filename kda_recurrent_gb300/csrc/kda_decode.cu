@@ -275,7 +275,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 // Shared-memory shape of the streaming schedule. A stage holds one item's state and the
 // q, k, g_raw, v rows of its `tokens` tokens; the stage count is whatever fits in
 // kStreamSmem (at most kMaxStages), so that 2-5 items are in flight per SM.
-template <typename T>
+template <typename T, bool kGroupLayout = sizeof(T) == 2>
 struct StreamShape {
     static constexpr int kMaxStages = 6;
     static constexpr uint32_t kItemBytes = kHeadDim * kHeadDim * sizeof(T);
@@ -283,8 +283,10 @@ struct StreamShape {
     static constexpr uint32_t kTokBytes = 4 * kHeadDim * 2;  // q, k, g_raw, v rows of one token
     static constexpr int VEC = StateVec<T>::kElems;
     static constexpr int RPP = kDecodeThreads / (kHeadDim / VEC);
-    // BF16 states are updated by two groups of four warps, one item each (see below)
-    static constexpr bool kGroups = sizeof(T) == 2;
+    // BF16 states with one token per row are updated by two groups of four warps, one item
+    // each (see below); FP32 states, and BF16 states with several tokens per row, by all eight
+    // compute warps, the state in FP32 registers for the whole row
+    static constexpr bool kGroups = kGroupLayout;
     static constexpr int kGroupBytes = 2 * 8 * kHeadDim * 4 + 4 * kHeadDim * 4 + kMaxTokensPerRow * 4;
     static constexpr int kRed = 2 * RPP * kHeadDim * 4;
     // FP32 states: the partial sums, u and beta, then the decay, k and q vectors of every
@@ -476,10 +478,10 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
 // would start the next item's load only once the compute warps want it, so each stage is
 // refilled as soon as its store has read it. With several tokens per row the state stays in
 // registers while its tokens are applied in order, and is stored once.
-template <typename T, bool kRefillAtOnce>
+template <typename T, bool kRefillAtOnce, bool kGroupLayout>
 __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kernel(DecodeArgs a) {
     using V = StateVec<T>;
-    using SS = StreamShape<T>;
+    using SS = StreamShape<T, kGroupLayout>;
     constexpr int VEC = V::kElems;
     constexpr int VPR = kHeadDim / VEC;
     constexpr int RPP = SS::RPP;
@@ -602,6 +604,7 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
 
     // ---- compute warps
     if constexpr (SS::kGroups) {
+        static_assert(sizeof(T) == 2, "the group layout is for BF16 states");
         stream_groups_bf16(a, stages, smem + NS * stage_bytes, NS, stage_bytes, full, done, first, stride, mine,
                            s_abort);
         return;
@@ -757,31 +760,46 @@ __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kern
     }
 }
 
-template <typename T, bool kRefillAtOnce>
+template <typename T, bool kRefillAtOnce, bool kGroupLayout>
 cudaError_t launch_decode_stream_t(const DecodeArgs &a, cudaStream_t stream, int sms) {
+    using SS = StreamShape<T, kGroupLayout>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kda_decode_stream_kernel<T, kRefillAtOnce>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, StreamShape<T>::kStreamSmem);
+        e = cudaFuncSetAttribute(kda_decode_stream_kernel<T, kRefillAtOnce, kGroupLayout>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SS::kStreamSmem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     const int64_t items = (int64_t)a.rows * a.num_heads;
     const int grid = (int)std::min<int64_t>(items, sms);
-    kda_decode_stream_kernel<T, kRefillAtOnce>
-        <<<grid, kDecodeThreads + 32, StreamShape<T>::smem(a.tokens), stream>>>(a);
+    kda_decode_stream_kernel<T, kRefillAtOnce, kGroupLayout>
+        <<<grid, kDecodeThreads + 32, SS::smem(a.tokens), stream>>>(a);
     return cudaGetLastError();
 }
 
+// Tokens per row from which BF16 states stay in registers for the whole row (measured on
+// 4096 rows x H8: the group layout is 29% faster at 2 tokens, 14% at 4, level at 8, 5%
+// slower at 16).
+constexpr int kBf16RowRegisterTokens = 8;
+
 template <typename T>
 cudaError_t launch_decode_stream(const DecodeArgs &a, cudaStream_t stream, int sms) {
-    // BF16 rings keep an even stage count of at least four
-    if constexpr (!StreamShape<T>::kGroups)
-        if (StreamShape<T>::stages(a.tokens) <= 2) return launch_decode_stream_t<T, true>(a, stream, sms);
-    return launch_decode_stream_t<T, false>(a, stream, sms);
+    if constexpr (sizeof(T) == 2) {
+        // up to 7 tokens per row: two compute groups on alternate items, the state in its stage
+        // (their rings keep an even stage count of at least four); from 8 on, where it is at
+        // least as fast, the state in FP32 registers for the whole row, rounded once
+        if (a.tokens >= kBf16RowRegisterTokens) {
+            if (StreamShape<T, false>::stages(a.tokens) <= 2) return launch_decode_stream_t<T, true, false>(a, stream, sms);
+            return launch_decode_stream_t<T, false, false>(a, stream, sms);
+        }
+        return launch_decode_stream_t<T, false, true>(a, stream, sms);
+    } else {
+        if (StreamShape<T>::stages(a.tokens) <= 2) return launch_decode_stream_t<T, true, false>(a, stream, sms);
+        return launch_decode_stream_t<T, false, false>(a, stream, sms);
+    }
 }
 
 template <typename T, int JW>
