@@ -28,6 +28,7 @@
 #include "kda_tc.cuh"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace kda {
 namespace {
@@ -77,6 +78,29 @@ struct StateVec<__nv_bfloat16> {
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
+
+// Four BF16 state elements (8 bytes): the vector of the streaming kernel's register layout
+// for BF16 states, which then has the FP32 layout's thread mapping (16 rows x 4 columns per
+// thread, 8 row partials per column sum).
+struct StateVecBF16x4 {
+    static constexpr int kElems = 4;
+    using Raw = uint2;
+    static __device__ __forceinline__ void unpack(const Raw &r, float (&x)[kElems]) {
+        x[0] = __uint_as_float(r.x << 16);
+        x[1] = __uint_as_float(r.x & 0xffff0000u);
+        x[2] = __uint_as_float(r.y << 16);
+        x[3] = __uint_as_float(r.y & 0xffff0000u);
+    }
+    static __device__ __forceinline__ Raw pack(const float (&x)[kElems]) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(x[0], x[1]), p1 = __floats2bfloat162_rn(x[2], x[3]);
+        return make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
+    }
+};
+
+// The state vector type of the streaming kernel: FP32 states and the BF16 group layout use
+// 16 bytes, the BF16 register layout 8.
+template <typename T, bool kGroupLayout>
+using StreamVec = typename std::conditional<sizeof(T) == 2 && !kGroupLayout, StateVecBF16x4, StateVec<T>>::type;
 
 // The two BF16 halves of a word as FP32 (low half first).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
@@ -281,7 +305,7 @@ struct StreamShape {
     static constexpr uint32_t kItemBytes = kHeadDim * kHeadDim * sizeof(T);
     static constexpr uint32_t kPiece = 16384;               // bytes per bulk copy of the state
     static constexpr uint32_t kTokBytes = 4 * kHeadDim * 2;  // q, k, g_raw, v rows of one token
-    static constexpr int VEC = StateVec<T>::kElems;
+    static constexpr int VEC = StreamVec<T, kGroupLayout>::kElems;
     static constexpr int RPP = kDecodeThreads / (kHeadDim / VEC);
     // BF16 states with one token per row are updated by two groups of four warps, one item
     // each (see below); FP32 states, and BF16 states with several tokens per row, by all eight
@@ -480,7 +504,7 @@ __device__ __forceinline__ void stream_groups_bf16(const DecodeArgs &a, uint8_t 
 // registers while its tokens are applied in order, and is stored once.
 template <typename T, bool kRefillAtOnce, bool kGroupLayout>
 __global__ void __launch_bounds__(kDecodeThreads + 32, 1) kda_decode_stream_kernel(DecodeArgs a) {
-    using V = StateVec<T>;
+    using V = StreamVec<T, kGroupLayout>;
     using SS = StreamShape<T, kGroupLayout>;
     constexpr int VEC = V::kElems;
     constexpr int VPR = kHeadDim / VEC;
@@ -781,16 +805,16 @@ cudaError_t launch_decode_stream_t(const DecodeArgs &a, cudaStream_t stream, int
 }
 
 // Tokens per row from which BF16 states stay in registers for the whole row (measured on
-// 4096 rows x H8: the group layout is 29% faster at 2 tokens, 14% at 4, level at 8, 5%
-// slower at 16).
-constexpr int kBf16RowRegisterTokens = 8;
+// 4096 rows x H8: the register layout is 17% slower at 2 tokens and 5% at 3, 6% faster at 4,
+// 18% at 6, 21% at 8, 24% at 16).
+constexpr int kBf16RowRegisterTokens = 4;
 
 template <typename T>
 cudaError_t launch_decode_stream(const DecodeArgs &a, cudaStream_t stream, int sms) {
     if constexpr (sizeof(T) == 2) {
-        // up to 7 tokens per row: two compute groups on alternate items, the state in its stage
-        // (their rings keep an even stage count of at least four); from 8 on, where it is at
-        // least as fast, the state in FP32 registers for the whole row, rounded once
+        // up to 3 tokens per row: two compute groups on alternate items, the state in its stage
+        // (their rings keep an even stage count of at least four); from 4 on, where it is
+        // faster, the state in FP32 registers for the whole row, rounded once
         if (a.tokens >= kBf16RowRegisterTokens) {
             if (StreamShape<T, false>::stages(a.tokens) <= 2) return launch_decode_stream_t<T, true, false>(a, stream, sms);
             return launch_decode_stream_t<T, false, false>(a, stream, sms);
