@@ -219,7 +219,10 @@ KDA_API int kda_decode(const void *q, const void *k, const void *v, const void *
  *   tokens_per_row  T in [1, KDA_DECODE_MAX_TOKENS]. Row r applies its T tokens in order to
  *                   pool slot slot_idx[r] (read once, written once). q, k, g_raw, v and out
  *                   are [rows, T, num_heads, 128]; beta is [rows, T, num_heads]. T = 1 is
- *                   kda_decode's layout. Larger T gives KDA_ERR_UNSUPPORTED.
+ *                   kda_decode's layout. Larger T gives KDA_ERR_UNSUPPORTED. A BF16 state
+ *                   is kept in FP32 between the row's tokens and rounded once when T >= 4;
+ *                   for T = 2, 3 it is rounded after every token, as T calls of kda_decode
+ *                   would round it.
  *   flags           bitwise OR of
  *                     KDA_DECODE_L2NORM_QK    q and k are first replaced, in FP32, by
  *                                             x * (sum x^2 + norm_eps)^-1/2
