@@ -190,12 +190,13 @@ def test_decode_and_windowed_prefill_replay_in_a_cuda_graph():
 
 
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("rows,tokens", [(3, 2), (600, 2), (40, 5), (300, 16), (900, 7)])
+@pytest.mark.parametrize("rows,tokens", [(3, 2), (600, 2), (200, 3), (200, 4), (40, 5), (300, 16), (900, 7)])
 def test_multi_token_decode_equals_prefill_of_short_sequences(state_dtype, rows, tokens):
     """T tokens per row applied in order to the row's slot: the oracle's prefill of T-token
     sequences started from the gathered pool states. Row 1 is a padding row. (900, 7) gives
     each CTA of the streaming schedule a dozen items with 3-15 tokens each, so every ring
-    stage is refilled several times (the BF16 ring then has an even stage count)."""
+    stage is refilled several times. BF16 states take the two-group layout up to 3 tokens
+    per row and the register layout from 4, so (200, 3) and (200, 4) straddle the switch."""
     H, slots_n = 2, 2048
     p = S.prefill_inputs([tokens] * rows, H, seed=50 + rows + tokens, init_std=None)
     shape4 = (rows, tokens, H, 128)
