@@ -31,7 +31,10 @@
 //               the output read-out and store; lane 0 of warps 12 and 13 issue the state
 //               MMAs, as two streams of independent accumulators.
 // Two stages of operands are in flight; the pair operands, the raw v and beta buffers and
-// TMEM's D1 buffers are each released as soon as their reader is done with them.
+// TMEM's D1 buffers are each released as soon as their reader is done with them. Group B
+// hands a chunk to the state warps in two steps: once V^T is in D1 and its Kt MMA is queued,
+// the state warps start the projection and the decay; once Kt and Bo are in the stage, the
+// output and update MMAs (queued behind the Kt MMA, the projection does not delay it).
 // Exponent range: per 16-token half, factors are anchored at the half's 8th token, built
 // as running products of the per-token decays and their inverses (no per-element exp of a
 // prefix); the off-diagonal block factors through the half boundary (both factors <= 1).
@@ -105,7 +108,7 @@ constexpr int kMq = kNt + 32 * kSq * 4;           // fp32 [32][36]: Mqk
 constexpr int kBetaS = kMq + 32 * kSq * 4;        // fp32 [32]: beta of the chunk
 constexpr int kQuart = kBetaS + 128;              // fp32 [4][128]: per-quarter decay products
 constexpr int kBars = kQuart + 4 * 128 * 4;
-constexpr int kSmemTc = kBars + 128;
+constexpr int kSmemTc = kBars + 256;
 static_assert(kStage0 % 128 == 0 && kStageBytes % 128 == 0 && kAtHi % 128 == 0, "operand alignment");
 constexpr int kSmemLaunch = kSmemTc + 1024;  // plus the alignment slack
 static_assert(kSmemLaunch <= 227 * 1024, "one CTA per SM");
@@ -122,6 +125,8 @@ constexpr uint32_t kIdescN32 = instr_desc(2, 128, 32);  // tf32, M128 N32
 
 struct Bars {
     uint64_t prep[2];    // group B -> state warps: stage s filled (count kSolveThreads)
+    uint64_t vready[2];  // group B -> state warps: V^T of the chunk of parity s in D1 (count
+                         //   kSolveThreads); the projection needs only that
     uint64_t g1;         // projection MMA complete (tcgen05.commit)
     uint64_t go;         // output MMA complete (tcgen05.commit)
     uint64_t g2;         // state update MMA complete (tcgen05.commit)
@@ -137,7 +142,7 @@ struct Bars {
     uint32_t tmem_base;
     int32_t abort;
 };
-static_assert(sizeof(Bars) <= 128, "barrier block");
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 // Programmatic dependent launch: let the next kernel of the stream start its launch now, and
 // wait until the previous kernel of the stream has completed and its writes are visible
@@ -697,6 +702,9 @@ __device__ void solve_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
             mma_commit(&B->kt);
         }
         __syncwarp();
+        // V^T is in D1 and the Kt MMA is queued ahead of the projection's: the state warps may
+        // start the chunk's projection
+        mbar_arrive(&B->vready[ps]);
         if (!kPass1) {
             // warp b: the 16 x 8 tiles (b / 2, 2 (b % 2)) and (b / 2, 2 (b % 2) + 1) of Bo; Bo is
             // lower triangular, so K steps outside [column tile, row tile] contribute nothing
@@ -828,7 +836,9 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         const int ps = c & 1, db = c & 1;
         const uint32_t cur = kColS;  // the state stays in one buffer, decayed in place
         const uint8_t *stage = smem + kStage0 + ps * kStageBytes;
-        if (!wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status)) break;
+        // the projection needs the chunk's operands (W, the decay), V^T in D1 and the previous
+        // update; Kt and Bo, which group B hands over later, only the output and update MMAs
+        if (!wait_or_abort(&B->vready[ps], (c >> 1) & 1, B, a.status)) break;
         if (c >= 1 && !wait_or_abort(&B->g2, (c - 1) & 1, B, a.status)) break;
         tc_fence_after();
         if (mma_thread) {
@@ -848,11 +858,12 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         }
         // the decay in place, once the projection has read the state (running it beside the
         // projection made both share the tensor memory's bandwidth)
-        const bool lost = !wait_or_abort(&B->g1, c & 1, B, a.status);
+        bool lost = !wait_or_abort(&B->g1, c & 1, B, a.status);
         tc_fence_after();
         if (!lost)
             decay_columns(tmem + lane_base + cur, tmem + lane_base + cur,
                           reinterpret_cast<const float *>(stage + kStDec), 4);
+        lost = lost || !wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status);  // Kt and Bo
         tc_fence_before();
         if (bar_any(kBarState, kStateThreads, lost)) break;
         tc_fence_after();
@@ -980,7 +991,8 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
     for (int c = 0; c < nchunks; ++c) {
         const int ps = c & 1, db = c & 1;
         const uint8_t *stage = smem + kStage0 + ps * kStageBytes;
-        if (!wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status)) break;
+        // the projections need V^T in D1 (and the chunk's operands); Kt only the updates
+        if (!wait_or_abort(&B->vready[ps], (c >> 1) & 1, B, a.status)) break;
         if (c >= 1 && !wait_or_abort(&B->g2, (c - 1) & 1, B, a.status)) break;
         tc_fence_after();
         // the S chain and the M chain from two warps, in parallel (both commit g1)
@@ -1002,7 +1014,11 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         // S and M are adjacent (columns [0, 256)): decay both in place
         decay_columns(tmem + lane_base + kColS, tmem + lane_base + kColS, reinterpret_cast<const float *>(stage + kStDec),
                       8);
-        tc_fence_before();
+        {
+            const bool lost = !wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status);  // Kt
+            tc_fence_before();
+            if (bar_any(kBarState, kStateThreads, lost)) break;
+        }
         mbar_arrive(&B->oread[db]);
         bar_named(kBarState, kStateThreads);
         tc_fence_after();
@@ -1159,6 +1175,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
     if (threadIdx.x == 0) {
         mbar_init(&B->prep[0], kSolveThreads);
         mbar_init(&B->prep[1], kSolveThreads);
+        mbar_init(&B->vready[0], kSolveThreads);
+        mbar_init(&B->vready[1], kSolveThreads);
         mbar_init(&B->ab_full[0], kProdThreads);
         mbar_init(&B->ab_full[1], kProdThreads);
         mbar_init(&B->ab_empty, kSolveThreads);
