@@ -28,8 +28,9 @@
 //               (I + Diag(beta) A)^-1 in FP32 by 16 x 16 blocks, T', the Kt MMA (tcgen05),
 //               Bo (mma.sync, TF32) and the hand-off of the stage;
 //   warps 12-15 state warps (one per TMEM lane quadrant): initial/final state, the decay,
-//               the output read-out and store; lane 0 of warps 12 and 13 issue the state
-//               MMAs, as two streams of independent accumulators.
+//               the output read-out and store; lane 0 of warp 12 issues the projection,
+//               lane 0 of warp 13 the update and then the output (in the window pass each
+//               issues one of the two chains).
 // Two stages of operands are in flight; the pair operands, the raw v and beta buffers and
 // TMEM's D1 buffers are each released as soon as their reader is done with them. Group B
 // hands a chunk to the state warps in two steps: once V^T is in D1 and its Kt MMA is queued,
@@ -867,17 +868,13 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         tc_fence_before();
         if (bar_any(kBarState, kStateThreads, lost)) break;
         tc_fence_after();
-        // O^T = (Qbar S)^T + R^T Bo^T and S^T += R^T Kt on the decayed state (A = R^T =
-        // D1^T[:, 0:32]): different accumulators, issued from two warps so that the two MMA
-        // streams go in parallel (one thread issues a tcgen05.mma only every ~90 cycles)
-        if (mma_thread) {
-            const uint32_t obase = smem_addr(stage + kStBo);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_tf32_ts(tmem + kColD1 + 64 * db + 32, tmem + kColD1 + 64 * db + 8 * s,
-                            smem_desc_kmajor(obase + 256 * s, 128, 1024), kIdescN32, true);
-            mma_commit(&B->go);
-        } else if (mma_thread2) {
+        // S^T += R^T Kt on the decayed state, then O^T = (Qbar S)^T + R^T Bo^T (A = R^T =
+        // D1^T[:, 0:32]), both from one thread: the update goes first, since the next chunk's
+        // projection waits for it; the output, which only its read-out waits for, queues behind
+        // it. (Issued from two threads at once, the two interleaved on the tensor pipe.) The
+        // stage is released with the update although the output MMAs still read Bo from it:
+        // nothing writes Bo there again before group B's wait for this chunk's read-out.
+        if (mma_thread2) {
             const uint32_t kbase = smem_addr(stage + kStKt);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
@@ -885,6 +882,12 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                             smem_desc_kmajor(kbase + 256 * s, 128, kKtSbo), kIdescG2, true);
             mma_commit(&B->g2);
             mma_commit(&B->g2s[ps]);
+            const uint32_t obase = smem_addr(stage + kStBo);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_tf32_ts(tmem + kColD1 + 64 * db + 32, tmem + kColD1 + 64 * db + 8 * s,
+                            smem_desc_kmajor(obase + 256 * s, 128, 1024), kIdescN32, true);
+            mma_commit(&B->go);
         }
         __syncwarp();
         // output read-out: O^T = D1^T[:, 32:64]
