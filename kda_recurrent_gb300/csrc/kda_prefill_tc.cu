@@ -16,9 +16,10 @@
 //     S = S Diag(2^G_last)                       (state warps, in TMEM, after the projection)
 //     S^T += R^T Kt                 M128 N128 K32, A = R^T read from TMEM
 // Kt^T = Kr^T T' is one more small tcgen05 product (M128 N32 K32, both operands in shared
-// memory, TF32), issued by the producers off the serial chain. The decay runs in place once the
-// projection has read the state: run beside the projection, the two shared the tensor memory's
-// bandwidth and the projection took several times its tensor-core time.
+// memory, TF32), issued by the producers off the serial chain. The decay runs in place, each
+// 32-column block of S^T once the projection's MMAs that read it are done: run beside the whole
+// projection into a second buffer, the two shared the tensor memory's bandwidth and the
+// projection took several times its tensor-core time.
 //
 // Warp roles (one CTA per (sequence, head) chain, 16 warps), a chunk per group in flight:
 //   warps 0-7   group A: raw loads (cp.async), gate and decay products, the pair operands
@@ -128,7 +129,7 @@ struct Bars {
     uint64_t prep[2];    // group B -> state warps: stage s filled (count kSolveThreads)
     uint64_t vready[2];  // group B -> state warps: V^T of the chunk of parity s in D1 (count
                          //   kSolveThreads); the projection needs only that
-    uint64_t g1;         // projection MMA complete (tcgen05.commit)
+    uint64_t g1q[4];     // the projection's MMAs that read S^T columns [32 q, 32 q + 32) complete
     uint64_t go;         // output MMA complete (tcgen05.commit)
     uint64_t g2;         // state update MMA complete (tcgen05.commit)
     uint64_t g2s[2];     // state update of a chunk on stage s complete (tcgen05.commit)
@@ -845,10 +846,11 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
         if (mma_thread) {
             const uint32_t wbase = smem_addr(stage + kStW);
 #pragma unroll
-            for (int s = 0; s < 16; ++s)
+            for (int s = 0; s < 16; ++s) {
                 mma_tf32_ts(tmem + kColD1 + 64 * db, tmem + cur + 8 * s,
                             smem_desc_sw128(wbase + (s >> 2) * 8192 + (s & 3) * 32), kIdescG1, true);
-            mma_commit(&B->g1);
+                if ((s & 3) == 3) mma_commit(&B->g1q[s >> 2]);  // S^T columns [8 s - 24, 8 s + 8) read
+            }
         }
         __syncwarp();
         if (c >= 1) {  // checkpoint of the state after chunk c-1 (read alongside the projection)
@@ -857,13 +859,18 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
                 store_state(tmem + cur, lane_base, dv,
                             a.ckpt + ((size_t)row * a.num_heads + h) * (kHeadDim * kHeadDim));
         }
-        // the decay in place, once the projection has read the state (running it beside the
-        // projection made both share the tensor memory's bandwidth)
-        bool lost = !wait_or_abort(&B->g1, c & 1, B, a.status);
-        tc_fence_after();
-        if (!lost)
-            decay_columns(tmem + lane_base + cur, tmem + lane_base + cur,
-                          reinterpret_cast<const float *>(stage + kStDec), 4);
+        // the decay in place, each 32-column block of S^T as soon as the projection's MMAs
+        // that read it are done, the rest of the projection still running (run beside the
+        // whole projection, into a second buffer, the two shared the tensor memory's bandwidth)
+        bool lost = false;
+#pragma unroll 1
+        for (int q = 0; q < 4 && !lost; ++q) {
+            lost = !wait_or_abort(&B->g1q[q], c & 1, B, a.status);
+            tc_fence_after();
+            if (!lost)
+                decay_columns(tmem + lane_base + cur + 32 * q, tmem + lane_base + cur + 32 * q,
+                              reinterpret_cast<const float *>(stage + kStDec) + 32 * q, 1);
+        }
         lost = lost || !wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status);  // Kt and Bo
         tc_fence_before();
         if (bar_any(kBarState, kStateThreads, lost)) break;
@@ -998,7 +1005,7 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         if (!wait_or_abort(&B->vready[ps], (c >> 1) & 1, B, a.status)) break;
         if (c >= 1 && !wait_or_abort(&B->g2, (c - 1) & 1, B, a.status)) break;
         tc_fence_after();
-        // the S chain and the M chain from two warps, in parallel (both commit g1)
+        // the S chain and the M chain from two warps, in parallel (both commit each g1q[q])
         if (mma_thread || mma_thread2) {
             const uint32_t wbase = smem_addr(stage + kStW);
             const uint32_t d = mma_thread ? kColD1 + 32 * db : kColD1M + 32 * db;
@@ -1008,17 +1015,25 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
                 const uint64_t bd = smem_desc_sw128(wbase + (s >> 2) * 8192 + (s & 3) * 32);
                 // D1 for S starts from V; D1 for M from zero
                 mma_tf32_ts(tmem + d, tmem + src + 8 * s, bd, kIdescN32, mma_thread || s > 0);
+                if ((s & 3) == 3) mma_commit(&B->g1q[s >> 2]);
             }
-            mma_commit(&B->g1);
         }
         __syncwarp();
-        if (!wait_or_abort(&B->g1, c & 1, B, a.status)) break;
-        tc_fence_after();
-        // S and M are adjacent (columns [0, 256)): decay both in place
-        decay_columns(tmem + lane_base + kColS, tmem + lane_base + kColS, reinterpret_cast<const float *>(stage + kStDec),
-                      8);
+        // decay S and M in place (columns [0, 128) and [128, 256)), each 32-column block as soon
+        // as both projections have read it
+        bool dlost = false;
+#pragma unroll 1
+        for (int q = 0; q < 4 && !dlost; ++q) {
+            dlost = !wait_or_abort(&B->g1q[q], c & 1, B, a.status);
+            tc_fence_after();
+            if (!dlost) {
+                const float *const dq = reinterpret_cast<const float *>(stage + kStDec) + 32 * q;
+                decay_columns(tmem + lane_base + kColS + 32 * q, tmem + lane_base + kColS + 32 * q, dq, 1);
+                decay_columns(tmem + lane_base + kColM + 32 * q, tmem + lane_base + kColM + 32 * q, dq, 1);
+            }
+        }
         {
-            const bool lost = !wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status);  // Kt
+            const bool lost = dlost || !wait_or_abort(&B->prep[ps], (c >> 1) & 1, B, a.status);  // Kt
             tc_fence_before();
             if (bar_any(kBarState, kStateThreads, lost)) break;
         }
@@ -1184,8 +1199,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         mbar_init(&B->ab_full[1], kProdThreads);
         mbar_init(&B->ab_empty, kSolveThreads);
         mbar_init(&B->vfree, kSolveThreads);
-        // the window pass's S and M chains are issued by two threads, which both commit
-        mbar_init(&B->g1, kPass1 ? 2 : 1);
         mbar_init(&B->go, 1);
         mbar_init(&B->kt, 1);
         mbar_init(&B->g2, kPass1 ? 2 : 1);
@@ -1194,6 +1207,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         mbar_init(&B->oread[0], kStateThreads);
         mbar_init(&B->oread[1], kStateThreads);
         mbar_init(&B->drain, 3);
+        for (int q = 0; q < 4; ++q) mbar_init(&B->g1q[q], kPass1 ? 2 : 1);
         B->abort = 0;
         fence_mbar_init();
     }
