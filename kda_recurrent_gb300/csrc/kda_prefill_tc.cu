@@ -1265,18 +1265,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
 // The dv columns of S are independent: each CTA carries 8 of them through all windows.
 // Warp p owns the 16 values of k in [16p, 16p + 16) and, per lane, 4 rows x 8 columns of
 // the product. The map arrives transposed (row k of M^T is column k of M), so a warp reads
-// 512 contiguous bytes per k; each register is refilled with the next window's value as
-// soon as this window's has been read. The 8 partial products are summed through shared
-// memory, and warp p also sums and rewrites rows [16p, 16p + 16) of S, the rows its next
-// window step reads, so one CTA barrier per window step suffices. The products run as
-// packed FP32 pairs of columns.
+// 512 contiguous bytes per k. The loads run two window steps ahead, in two register sets
+// that alternate between steps: each register is refilled with the map of window w + 2 as
+// soon as window w's value has been read (one step ahead, the steps waited on the loads).
+// The 8 partial products are summed through shared memory, in the order of the slices, and
+// warp p also sums and rewrites rows [16p, 16p + 16) of S, the rows its next window step
+// reads, so one CTA barrier per window step suffices. The products run as packed FP32
+// pairs of columns.
 constexpr int kCarryCols = 8;
 constexpr int kCarryWarps = kHeadDim / 16;
 constexpr int kCarryThreads = 32 * kCarryWarps;
-
 // Partial products, double-buffered by window step: [buffer][slice][column][row], rows padded
-// to 132 floats so that the two column halves a warp reads at once fall in different banks.
-constexpr int kCarryRowPad = kHeadDim + 4;
+// to 144 floats, so that columns c and c + 1 start 64 bytes apart in the banks and a warp's
+// 16-byte reads of 8 columns x 4 rows take the minimum 4 wavefronts.
+constexpr int kCarryRowPad = kHeadDim + 16;
 constexpr int kCarryDynSmem = 2 * kCarryWarps * kCarryCols * kCarryRowPad * 4;
 
 __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const PrefillArgs a) {
@@ -1289,30 +1291,41 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     const int c0 = (blockIdx.x - lc * blocks) * kCarryCols;
     pdl_launch_dependents();  // the output pass may start now; it waits for this grid on the device
     const int n = seq_of_rank(a, pos / a.num_heads, reinterpret_cast<int *>(carry_dyn));
-    const int chain = n * a.num_heads + pos % a.num_heads;
-    (void)chain;
     const WindowSpan sp = window_span(a, n, 0, a.wins, false);
     if (sp.wins_seq <= 2) return;  // window 1's start state comes from window 0 itself
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int k0 = 16 * warp;
-    // warp w multiplies rows [k0, k0 + 16) of S and also reduces and rewrites exactly those
+    const int rq = lane & 3, cc = lane >> 2;
+    // warp p multiplies rows [k0, k0 + 16) of S and also reduces and rewrites exactly those
     // rows, so between window steps it waits only for its own lanes
-    const int rr = k0 + (lane & 15), ch = lane >> 4;  // reduction: row rr, columns 4 ch .. 4 ch + 3
-    *reinterpret_cast<float4 *>(&S[rr][4 * ch]) =
-        __ldcg(reinterpret_cast<const float4 *>(window_slot(a, lc, 1, 0) + (size_t)rr * kHeadDim + c0 + 4 * ch));
-    float4 mv[16];  // M^T[k0 + kk][4 lane .. 4 lane + 3]
+    const int r4 = k0 + 4 * rq;  // reduction: rows r4 .. r4 + 3, column cc
+    {
+        const float *const src = window_slot(a, lc, 1, 0) + (size_t)r4 * kHeadDim + c0 + cc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S[r4 + i][cc] = __ldcg(src + i * kHeadDim);
+    }
     auto map_row = [&](int w, int kk) {
         return reinterpret_cast<const float4 *>(window_slot(a, lc, w, 2) + (size_t)(k0 + kk) * kHeadDim + 4 * lane);
     };
+    float e[4];
     auto load_e = [&](int w) {
-        return __ldcg(reinterpret_cast<const float4 *>(window_slot(a, lc, w, 1) + (size_t)rr * kHeadDim + c0 + 4 * ch));
-    };
+        const float *const src = window_slot(a, lc, w, 1) + (size_t)r4 * kHeadDim + c0 + cc;
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) mv[kk] = __ldcg(map_row(1, kk));
-    float4 e4 = load_e(1);
+        for (int i = 0; i < 4; ++i) e[i] = __ldcg(src + i * kHeadDim);
+    };
+    // ma, mb: M^T[k0 + kk][4 lane .. 4 lane + 3] of windows w (set (w - 1) % 2) and w + 1
+    float4 ma[16], mb[16];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) ma[kk] = __ldcg(map_row(1, kk));
+    if (sp.wins_seq >= 4) {
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) mb[kk] = __ldcg(map_row(2, kk));
+    }
+    load_e(1);
     __syncwarp();
-    for (int w = 1; w + 1 < sp.wins_seq; ++w) {
+    auto step = [&](int w, float4 (&mv)[16]) {
         const int b = w & 1;
+        const bool ahead = w + 3 < sp.wins_seq;  // window w + 2 has a map
         float acc[4][kCarryCols];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -1325,7 +1338,7 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
             const float2 sv[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
                                   make_float2(s1.z, s1.w)};
             const float m[4] = {mv[kk].x, mv[kk].y, mv[kk].z, mv[kk].w};
-            if (w + 2 < sp.wins_seq) mv[kk] = __ldcg(map_row(w + 1, kk));  // next window's row, a step ahead
+            if (ahead) mv[kk] = __ldcg(map_row(w + 2, kk));
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -1341,16 +1354,28 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
             *reinterpret_cast<float4 *>(&part[b][warp][c][4 * lane]) =
                 make_float4(acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
         __syncthreads();  // every slice's partial products of step w are written
-        float sum[4] = {e4.x, e4.y, e4.z, e4.w};
-        if (w + 2 < sp.wins_seq) e4 = load_e(w + 1);
+        float sum[4] = {e[0], e[1], e[2], e[3]};
+        if (w + 2 < sp.wins_seq) load_e(w + 1);
 #pragma unroll
-        for (int p = 0; p < kCarryWarps; ++p)
+        for (int p = 0; p < kCarryWarps; ++p) {
+            const float4 x = *reinterpret_cast<const float4 *>(&part[b][p][cc][r4]);
+            sum[0] += x.x, sum[1] += x.y, sum[2] += x.z, sum[3] += x.w;
+        }
+        float *const out = window_slot(a, lc, w + 1, 0) + (size_t)r4 * kHeadDim + c0 + cc;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) sum[c] += part[b][p][4 * ch + c][rr];
-        const float4 s4 = make_float4(sum[0], sum[1], sum[2], sum[3]);
-        *reinterpret_cast<float4 *>(&S[rr][4 * ch]) = s4;
-        *reinterpret_cast<float4 *>(window_slot(a, lc, w + 1, 0) + (size_t)rr * kHeadDim + c0 + 4 * ch) = s4;
+        for (int i = 0; i < 4; ++i) {
+            S[r4 + i][cc] = sum[i];
+            out[i * kHeadDim] = sum[i];
+        }
         __syncwarp();  // this warp's rows of S are rewritten
+    };
+    for (int w = 1;;) {  // two steps per turn, so that each names its register set statically
+        if (w + 1 >= sp.wins_seq) break;
+        step(w, ma);
+        ++w;
+        if (w + 1 >= sp.wins_seq) break;
+        step(w, mb);
+        ++w;
     }
 }
 
