@@ -566,10 +566,11 @@ __device__ void producer_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint
                 } else {
                     st_pair(pairKR, (32 + i) * kRowB + ch, mul2(k2, mul2(S[ii], od)));
                 }
-                // 2^G_i and 2^(G_L - G_i)
-                *reinterpret_cast<float2 *>(stage + kStW + w_off(i, ch)) = mul2(k2, mul2(npreT, P[ii]));
-                if (!kPass1)
-                    *reinterpret_cast<float2 *>(stage + kStW + w_off(32 + i, ch)) = mul2(q2, mul2(preT, P[ii]));
+                // 2^G_i and 2^(G_L - G_i); row 32 + i lies 4096 bytes after row i (the same
+                // swizzle phase), so both stores share one offset
+                uint8_t *const wrow = stage + kStW + w_off(i, ch);
+                *reinterpret_cast<float2 *>(wrow) = mul2(k2, mul2(npreT, P[ii]));
+                if (!kPass1) *reinterpret_cast<float2 *>(wrow + 4096) = mul2(q2, mul2(preT, P[ii]));
                 kr[ii] = mul2(k2, mul2(S[ii], postT));
             }
 #pragma unroll
