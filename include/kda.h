@@ -173,8 +173,9 @@ KDA_API int kda_prefill_ex(const void *q, const void *k, const void *v, const vo
  *     call writes every scratch byte it reads before reading it, so stale contents from
  *     an earlier call never matter.
  *   - A shape whose window plan needs more than KDA_NOALLOC_SCRATCH_BYTES returns
- *     KDA_ERR_UNSUPPORTED. A plan needs at most (3 * SMs - 2) * 64 KiB, so every plan
- *     fits on GPUs with up to 171 SMs (GB300, 152 SMs: at most 28.4 MiB).
+ *     KDA_ERR_UNSUPPORTED. A plan needs at most (3 * SMs - 2) * 64 KiB plus under 1 KiB
+ *     of per-window flags, so every plan fits on GPUs with up to 171 SMs (GB300, 152 SMs:
+ *     at most 28.4 MiB).
  *   - Shapes that need no windows run the sequential schedule, as kda_prefill.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -88,6 +88,11 @@ constexpr int64_t kStateBytes = 128LL * 128 * 4;
 // Slots of one windowed chain with `wins` windows: start states of windows 1 .. wins - 1, and
 // E and M of windows 1 .. wins - 2.
 __host__ __device__ constexpr int64_t window_slots(int64_t wins) { return 3 * wins - 5; }
+// After the state slots of all windowed chains: one int32 per (windowed chain, window), set by
+// the window pass to whether the window's map M has a nonzero entry, padded to 256 bytes.
+__host__ __device__ constexpr int64_t window_flag_bytes(int64_t chains, int64_t wins) {
+    return (chains * wins * 4 + 255) / 256 * 256;
+}
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);  // windows when a.wins > 1

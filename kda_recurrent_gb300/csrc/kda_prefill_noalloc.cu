@@ -23,9 +23,10 @@ namespace {
 
 // Scratch of the window schedule: 32 MiB. A plan on a GPU with `sms` multiprocessors windows
 // the last `tail` chains (tail <= sms / 3) into W <= sms / tail + 1 windows each, and each
-// windowed chain needs 3W - 5 FP32 states of 64 KiB. So a plan needs at most
-// tail (3W - 5) <= 3 sms - 2 tail <= 3 sms - 2 states: 454 states (28.4 MiB) on GB300's
-// 152 SMs, and the 512 states of this array cover every plan up to 171 SMs.
+// windowed chain needs 3W - 5 FP32 states of 64 KiB, plus one int32 flag per window. So a
+// plan needs at most tail (3W - 5) <= 3 sms - 2 tail <= 3 sms - 2 states (454 states,
+// 28.4 MiB, on GB300's 152 SMs) and tail W <= sms + tail flags (under 1 KiB); the 512 states
+// of this array cover every plan up to 171 SMs.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;

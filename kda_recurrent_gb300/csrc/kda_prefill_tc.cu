@@ -975,7 +975,7 @@ __device__ void state_loop(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_
 constexpr uint32_t kColM = 128;
 constexpr uint32_t kColD1M = 320;
 __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, uint32_t tmem, int nchunks,
-                                 float *E_out, float *Mt_out) {
+                                 float *E_out, float *Mt_out, int *map_nonzero) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;
     const int row = 32 * quad + lane;
@@ -1055,7 +1055,10 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         if (bar_any(kBarState, kStateThreads, B->abort != 0)) break;
     }
     if (bar_any(kBarState, kStateThreads, B->abort != 0)) return;
-    if (nchunks > 0 && !wait_or_abort(&B->g2, (nchunks - 1) & 1, B, a.status)) return;
+    {  // one decision for all: the map flag below is reduced over a barrier of these threads
+        const bool lost = nchunks > 0 && !wait_or_abort(&B->g2, (nchunks - 1) & 1, B, a.status);
+        if (bar_any(kBarState, kStateThreads, lost)) return;
+    }
     tc_fence_after();
     // E[dk][dv] from S^T (lane dv, column dk); the map is stored transposed, M^T[dk'][dk],
     // straight from its TMEM rows (lane dk', column dk), which is the order the carry reads.
@@ -1067,6 +1070,7 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
 #pragma unroll
         for (int e = 0; e < 16; ++e) E_out[(16 * j + e) * kHeadDim + row] = v[e];
     }
+    bool nz = false;
 #pragma unroll 1
     for (int j = 0; j < 8; ++j) {
         float v[16];
@@ -1075,7 +1079,12 @@ __device__ void state_loop_pass1(const PrefillArgs &a, uint8_t *smem, Bars *B, u
         float4 *dst = reinterpret_cast<float4 *>(Mt_out + (size_t)row * kHeadDim + 16 * j);
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4) dst[e4] = make_float4(v[4 * e4], v[4 * e4 + 1], v[4 * e4 + 2], v[4 * e4 + 3]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) nz = nz || v[e] != 0.0f;
     }
+    // (NaN counts as nonzero)
+    const bool any_nz = bar_any(kBarState, kStateThreads, nz);
+    if (threadIdx.x == kFirstStateWarp * 32) *map_nonzero = any_nz ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1156,6 +1165,14 @@ __device__ __forceinline__ float *window_slot(const PrefillArgs &a, int lc, int 
     return a.ws + ((size_t)lc * (size_t)window_slots(W) + (size_t)idx) * (kHeadDim * kHeadDim);
 }
 
+// Whether window w of windowed chain lc has a map with a nonzero entry (written by the window
+// pass; a map whose every entry underflowed to zero makes the carry's step S = E).
+__device__ __forceinline__ int *window_flag(const PrefillArgs &a, int lc, int w) {
+    const int64_t chains = (int64_t)a.num_seqs * a.num_heads - a.seq_chains;
+    int *const flags = reinterpret_cast<int *>(a.ws + (size_t)chains * (size_t)window_slots(a.wins) * (kHeadDim * kHeadDim));
+    return flags + (size_t)lc * a.wins + w;
+}
+
 template <bool kPass1>
 __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1227,7 +1244,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
         solve_loop<kPass1>(a, smem, B, tmem, nchunks);
     } else {
         if (kPass1) {
-            state_loop_pass1(a, smem, B, tmem, nchunks, window_slot(a, lc, w, 1), window_slot(a, lc, w, 2));
+            state_loop_pass1(a, smem, B, tmem, nchunks, window_slot(a, lc, w, 1), window_slot(a, lc, w, 2),
+                             window_flag(a, lc, w));
         } else {
             // the start state of a window is the carry's output; the operand and solve warps
             // read only the inputs and start before the carry has finished
@@ -1282,8 +1300,11 @@ constexpr int kCarryThreads = 32 * kCarryWarps;
 constexpr int kCarryRowPad = kHeadDim + 16;
 constexpr int kCarryDynSmem = 2 * kCarryWarps * kCarryCols * kCarryRowPad * 4;
 
+constexpr int kCarryFlagWins = 256;  // windows whose map flag the carry keeps; later ones count as nonzero
+
 __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const PrefillArgs a) {
     __shared__ __align__(16) float S[kHeadDim][kCarryCols];
+    __shared__ int s_nz[kCarryFlagWins];
     extern __shared__ __align__(16) float carry_dyn[];
     auto part = reinterpret_cast<float (*)[kCarryWarps][kCarryCols][kCarryRowPad]>(carry_dyn);
     const int blocks = kHeadDim / kCarryCols;
@@ -1294,7 +1315,33 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     const int n = seq_of_rank(a, pos / a.num_heads, reinterpret_cast<int *>(carry_dyn));
     const WindowSpan sp = window_span(a, n, 0, a.wins, false);
     if (sp.wins_seq <= 2) return;  // window 1's start state comes from window 0 itself
+    const int last = sp.wins_seq - 2;  // the steps run over the windows with a map
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // which maps have a nonzero entry: a step whose map underflowed to zero everywhere is
+    // S_start[w+1] = E_w, and neither its map nor the product is needed
+    for (int t = 1 + tid; t <= last && t < kCarryFlagWins; t += kCarryThreads) s_nz[t] = __ldcg(window_flag(a, lc, t));
+    __syncthreads();
+    auto nonzero = [&](int w) { return w >= kCarryFlagWins || s_nz[w] != 0; };
+    {
+        bool any = false;
+        for (int w = 1; w <= last; ++w) any = any || nonzero(w);
+        if (!any) {
+            // every map is zero (fast decay over a window): each start state is the previous
+            // window's end state, S_start[w+1] = E_w, independent of the others, so the copies
+            // go out 8 windows at a time; thread t moves row t / 2, columns 4 (t % 2) .. + 3
+            const size_t off = (size_t)(tid >> 1) * kHeadDim + c0 + 4 * (tid & 1);
+            for (int w0 = 1; w0 <= last; w0 += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (w0 + j <= last) v[j] = __ldcg(reinterpret_cast<const float4 *>(window_slot(a, lc, w0 + j, 1) + off));
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (w0 + j <= last) *reinterpret_cast<float4 *>(window_slot(a, lc, w0 + j + 1, 0) + off) = v[j];
+            }
+            return;
+        }
+    }
     const int k0 = 16 * warp;
     const int rq = lane & 3, cc = lane >> 2;
     // warp p multiplies rows [k0, k0 + 16) of S and also reduces and rewrites exactly those
@@ -1316,9 +1363,11 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     };
     // ma, mb: M^T[k0 + kk][4 lane .. 4 lane + 3] of windows w (set (w - 1) % 2) and w + 1
     float4 ma[16], mb[16];
+    if (nonzero(1)) {
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) ma[kk] = __ldcg(map_row(1, kk));
-    if (sp.wins_seq >= 4) {
+        for (int kk = 0; kk < 16; ++kk) ma[kk] = __ldcg(map_row(1, kk));
+    }
+    if (last >= 2 && nonzero(2)) {
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) mb[kk] = __ldcg(map_row(2, kk));
     }
@@ -1326,7 +1375,26 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
     __syncwarp();
     auto step = [&](int w, float4 (&mv)[16]) {
         const int b = w & 1;
-        const bool ahead = w + 3 < sp.wins_seq;  // window w + 2 has a map
+        const bool ahead = w + 2 <= last && nonzero(w + 2);  // window w + 2's map is needed
+        if (!nonzero(w)) {  // S_start[w+1] = E_w
+            if (ahead) {
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) mv[kk] = __ldcg(map_row(w + 2, kk));
+            }
+            // one CTA barrier per step, as in a product step, so that the two partial-sum
+            // buffers keep alternating safely
+            __syncthreads();
+            const float sum[4] = {e[0], e[1], e[2], e[3]};
+            if (w + 1 <= last) load_e(w + 1);
+            float *const out = window_slot(a, lc, w + 1, 0) + (size_t)r4 * kHeadDim + c0 + cc;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                S[r4 + i][cc] = sum[i];
+                out[i * kHeadDim] = sum[i];
+            }
+            __syncwarp();  // this warp's rows of S are rewritten
+            return;
+        }
         float acc[4][kCarryCols];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -1356,7 +1424,7 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
                 make_float4(acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
         __syncthreads();  // every slice's partial products of step w are written
         float sum[4] = {e[0], e[1], e[2], e[3]};
-        if (w + 2 < sp.wins_seq) load_e(w + 1);
+        if (w + 1 <= last) load_e(w + 1);
 #pragma unroll
         for (int p = 0; p < kCarryWarps; ++p) {
             const float4 x = *reinterpret_cast<const float4 *>(&part[b][p][cc][r4]);
@@ -1371,10 +1439,10 @@ __global__ void __launch_bounds__(kCarryThreads) kda_window_carry_kernel(const P
         __syncwarp();  // this warp's rows of S are rewritten
     };
     for (int w = 1;;) {  // two steps per turn, so that each names its register set statically
-        if (w + 1 >= sp.wins_seq) break;
+        if (w > last) break;
         step(w, ma);
         ++w;
-        if (w + 1 >= sp.wins_seq) break;
+        if (w > last) break;
         step(w, mb);
         ++w;
     }
@@ -1418,7 +1486,7 @@ WindowPlan plan_windows(int32_t num_seqs, int32_t total_tokens, int32_t num_head
     const int64_t wins = std::min<int64_t>(sms / tail + 1, max_chunks / kMinWindowChunks);
     if (wins < 3) return p;
     p.wins = (int32_t)wins;
-    p.ws_bytes = tail * window_slots(wins) * kStateBytes;
+    p.ws_bytes = tail * window_slots(wins) * kStateBytes + window_flag_bytes(tail, wins);
     p.seq_chains = (int32_t)(chains - tail);
     return p;
 }

@@ -165,21 +165,27 @@ def test_product_path_has_no_fallback(monkeypatch, tmp_path):
         K.load()
 
 
+def flags(chains, wins):
+    """Bytes of the per-window map flags after the state slots (one int32 per window, 256-byte padded)."""
+    return (chains * wins * 4 + 255) // 256 * 256
+
+
 def test_window_plan_on_host(lib):
     """kda_prefill_workspace_size with an explicit SM count is host arithmetic only."""
     slot = 128 * 128 * 4  # one FP32 state; a chain with W windows keeps 3 W - 5 of them
-    assert K.kda_prefill_workspace_size(1, 8192, 8, sm_count=152) == 8 * 55 * slot    # 8 chains x 20 windows
-    assert K.kda_prefill_workspace_size(1, 512, 8, sm_count=152) == 8 * 7 * slot      # 16 chunks: 4 windows of 4
-    assert K.kda_prefill_workspace_size(16, 25729, 32, sm_count=152) == 0             # 512 chains fill the GPU
-    assert K.kda_prefill_workspace_size(8, 131072, 96, sm_count=152) == 8 * 55 * slot  # 5 full waves + 8 chains
-    assert K.kda_prefill_workspace_size(2, 8192, 76, sm_count=152) == 0               # exactly one full wave
-    assert K.kda_prefill_workspace_size(1, 8192, 204, sm_count=152) == 0              # 52-chain tail: > a third
-    assert K.kda_prefill_workspace_size(1, 8192, 202, sm_count=152) == 50 * 7 * slot  # 50-chain tail, 4 windows
-    assert K.kda_prefill_workspace_size(1, 64, 1, sm_count=152) == 0                 # 2 chunks: no windows
+    size = K.kda_prefill_workspace_size
+    assert size(1, 8192, 8, sm_count=152) == 8 * 55 * slot + flags(8, 20)    # 8 chains x 20 windows
+    assert size(1, 512, 8, sm_count=152) == 8 * 7 * slot + flags(8, 4)      # 16 chunks: 4 windows of 4
+    assert size(16, 25729, 32, sm_count=152) == 0                           # 512 chains fill the GPU
+    assert size(8, 131072, 96, sm_count=152) == 8 * 55 * slot + flags(8, 20)  # 5 full waves + 8 chains
+    assert size(2, 8192, 76, sm_count=152) == 0                             # exactly one full wave
+    assert size(1, 8192, 204, sm_count=152) == 0                            # 52-chain tail: > a third
+    assert size(1, 8192, 202, sm_count=152) == 50 * 7 * slot + flags(50, 4)  # 50-chain tail, 4 windows
+    assert size(1, 64, 1, sm_count=152) == 0                               # 2 chunks: no windows
     # a small GPU: W = min(SMs / tail + 1, chunks / 4) windows for a tail of at most SMs / 3
-    assert K.kda_prefill_workspace_size(1, 1024, 1, sm_count=8) == 1 * 19 * slot      # W = 8
-    assert K.kda_prefill_workspace_size(3, 3000, 1, sm_count=8) == 0                 # tail 3 > 8 / 3
-    assert K.kda_prefill_workspace_size(10, 64000, 1, sm_count=8) == 2 * 10 * slot    # 8 + 2 chains, W = 5
+    assert size(1, 1024, 1, sm_count=8) == 1 * 19 * slot + flags(1, 8)      # W = 8
+    assert size(3, 3000, 1, sm_count=8) == 0                               # tail 3 > 8 / 3
+    assert size(10, 64000, 1, sm_count=8) == 2 * 10 * slot + flags(2, 5)    # 8 + 2 chains, W = 5
     assert K.kda_prefill_workspace_size(1, 352, 2, sm_count=152) == 0                 # 11 chunks: W would be 2
     assert K.kda_prefill_workspace_size(0, 0, 1, sm_count=152) == 0
     with pytest.raises(K.KdaError):
@@ -189,8 +195,9 @@ def test_window_plan_on_host(lib):
 
 
 def test_noalloc_scratch_bound_on_host(lib):
-    """Every window plan needs at most 3 SMs - 2 FP32 states, so the fixed 32 MiB array of
-    kda_prefill_noalloc holds every plan on GPUs of up to 171 SMs (host arithmetic only)."""
+    """Every window plan needs at most 3 SMs - 2 FP32 states (and under 1 KiB of map flags), so
+    the fixed 32 MiB array of kda_prefill_noalloc holds every plan on GPUs of up to 171 SMs
+    (host arithmetic only)."""
     slot = 128 * 128 * 4
     for sms in (8, 76, 148, 152, 160, 171):
         worst = 0
@@ -199,6 +206,6 @@ def test_noalloc_scratch_bound_on_host(lib):
             seqs = sms + tail
             toks = seqs * (sms // tail + 1) * 4 * 32
             worst = max(worst, K.kda_prefill_workspace_size(seqs, toks, 1, sm_count=sms))
-        assert worst == (3 * sms - 2) * slot, sms  # reached by a tail of one chain
+        assert worst == (3 * sms - 2) * slot + flags(1, sms + 1), sms  # reached by a tail of one chain
         assert worst <= K.KDA_NOALLOC_SCRATCH_BYTES
     assert (3 * 172 - 2) * slot > K.KDA_NOALLOC_SCRATCH_BYTES

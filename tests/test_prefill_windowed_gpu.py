@@ -155,7 +155,7 @@ def test_windowed_tail_after_full_waves():
 def test_windowed_three_windows_minimum():
     """13 chunks on 2 chains: the smallest plan, windows 0, 1 and 2 of 5, 5 and 3 chunks
     (window 0 from the initial state, one window pass, one carry step)."""
-    assert K.kda_prefill_workspace_size(1, 400, 2, sm_count=152) == 2 * 4 * 128 * 128 * 4
+    assert K.kda_prefill_workspace_size(1, 400, 2, sm_count=152) == 2 * 4 * 128 * 128 * 4 + 256  # + map flags
     inp = S.prefill_inputs([400], 2, seed=36, init_std=0.02)
     check(inp, lower_bound=-5.0, gate_mode="lower_bound")
 
