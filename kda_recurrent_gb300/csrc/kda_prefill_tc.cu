@@ -1290,7 +1290,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) kda_prefill_tc_kernel(const Pre
 // The 8 partial products are summed through shared memory, in the order of the slices, and
 // warp p also sums and rewrites rows [16p, 16p + 16) of S, the rows its next window step
 // reads, so one CTA barrier per window step suffices. The products run as packed FP32
-// pairs of columns.
+// pairs of columns. A window whose map underflowed to zero everywhere (the window pass
+// records a flag per window) contributes S_start[w+1] = E_w: its map is neither loaded nor
+// multiplied, and a chain with only such windows copies its start states in one pass.
 constexpr int kCarryCols = 8;
 constexpr int kCarryWarps = kHeadDim / 16;
 constexpr int kCarryThreads = 32 * kCarryWarps;
