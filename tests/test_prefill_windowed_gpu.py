@@ -66,6 +66,34 @@ def test_windowed_slow_decay_carries_the_state(rate):
     check(inp, lower_bound=0.0, gate_mode="log_decay")
 
 
+def test_windowed_maps_zero_in_some_windows_only():
+    """Slow decay, then g = -5 per token over tokens 1000-1999, then slow decay again: the maps
+    of the windows inside the fast stretch underflow to zero and the others do not, so the
+    carry mixes product steps with steps that take S_start[w+1] = E_w."""
+    inp = S.prefill_inputs([3000], 2, seed=39, init_std=0.02)
+    g = -0.002 * inp["g_raw"].float().abs()
+    g[1000:2000] = -5.0
+    inp["g_raw"] = g.to(torch.bfloat16)
+    d = to_dev(inp)
+    ws = K.prefill_workspace(1, 3000, 2, DEV)
+    out, fin = K.prefill(d["q"], d["k"], d["v"], d["g_raw"], d["beta"], d["cu_seqlens"], d["init_state"],
+                         scale=SCALE, lower_bound=0.0, gate_mode="log_decay", workspace=ws)
+    st, detail = K.kda_device_status()
+    assert st == K.KDA_OK, (st, detail)
+    # the per-window map flags after the state slots: 2 chains, W windows each; this sequence
+    # has 94 chunks in windows of ceil(94 / W) chunks, and windows 1 .. wins - 2 carry a map
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    W = min(sms // 2 + 1, 94 // 4)
+    lw = -(-94 // W)
+    wins = -(-94 // lw)
+    off = 2 * (3 * W - 5) * 128 * 128 * 4
+    flags = ws[off:off + 2 * W * 4].view(torch.int32).view(2, W)[:, 1:wins - 1].cpu()
+    assert (flags == 0).any() and (flags == 1).any(), flags
+    ref_out, ref_fin = oracle_prefill(inp, scale=SCALE, lower_bound=0.0, gate_mode="log_decay")
+    assert_out_close(out.cpu(), ref_out)
+    assert_state_close(fin.cpu(), ref_fin)
+
+
 @pytest.mark.parametrize("lens", [[3000], [1500, 3000, 610]], ids=["1x3000", "varlen3"])
 def test_windowed_lower_bound_minus_8(lens):
     """lb = -8, the widest exponent range of the half-chunk anchors, on the window schedule with
